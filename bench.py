@@ -1,0 +1,382 @@
+"""Benchmark of the draft-head decode step on GB300.
+
+Workload (one step): the full-vocabulary bf16 head W [163840 x 4096] (1.34 GB, larger than L2, so
+no flush is needed) against 1, 5, 10 and 15 activation rows, each call writing fp32 logits and the
+fused top-1 over vocabulary parts plus a join; 1% of the head's rows are planted exact copies.
+The metric is achieved HBM GB/s (algorithmic bytes / time) and us per call; the FP8 head
+(E4M3 + E8M0 32x32 blocks, and per-row scales) with fused top-64 is reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (the plain fp64 restatement in oracle/) on a bounded
+sample of the same workload. Under torchrun every rank runs its own replica (weak scaling); rank 0
+prints one JSON line.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+VOCAB, HIDDEN = 163840, 4096
+ROWS = (1, 5, 10, 15)
+METRIC = "head GEMV+top-k achieved HBM GB/s (% of peak) and us/call at 1/5/10/15 rows"
+WORKLOAD = ("full-vocab bf16 head 163840x4096, rows 1/5/10/15, fp32 logits + fused top-1 over "
+            "vocabulary parts and a join, 1% planted exact-tie rows")
+
+
+def bf16_call_bytes(rows):
+    """Algorithmic bytes of one bf16 call: weights once, activations, fp32 logits, top-1."""
+    return VOCAB * HIDDEN * 2 + rows * HIDDEN * 2 + rows * VOCAB * 4 + rows * 8
+
+
+def fp8_call_bytes(rows, k=64):
+    """FP8 call without logits: codes, scales (655,360 B either form), activations, top-k."""
+    return VOCAB * HIDDEN + 655360 + rows * HIDDEN * 2 + rows * k * 8
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        return None
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle timing (the reported baseline and the reference arm)
+# ---------------------------------------------------------------------------------------------
+SAMPLE_ROWS = 16384  # vocabulary rows of the oracle's sample (1/10 of the head)
+
+
+def oracle_sample_worker(seconds):
+    """Times the oracle (as it stands) on a slice of the workload; prints one JSON line."""
+    import numpy as np
+
+    from oracle import gemv as og
+    from oracle.topk import topk
+    from synth import inputs
+
+    w = inputs.normal_bf16((SAMPLE_ROWS, HIDDEN), 0.02, 1).float().numpy()
+    x = inputs.rows(16).float().numpy()
+    t0 = time.perf_counter()
+    nbytes = 0
+    calls = 0
+    while True:
+        for r in ROWS:
+            y = og.gemv(w, x[:r], og.W_BF16, None, og.OUT_F32)
+            topk(y, 1)
+            nbytes += SAMPLE_ROWS * HIDDEN * 2 + r * HIDDEN * 2 + r * SAMPLE_ROWS * 4 + r * 8
+            calls += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    print(json.dumps({"gbs": nbytes / dt / 1e9, "seconds": dt, "calls": calls,
+                      "threads": int(os.environ.get("OPENBLAS_NUM_THREADS", "0") or 0)}))
+
+
+def run_oracle_sample(seconds):
+    threads = os.cpu_count() or 1
+    env = dict(os.environ, OPENBLAS_NUM_THREADS=str(threads), OMP_NUM_THREADS=str(threads),
+               MKL_NUM_THREADS=str(threads))
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker",
+                          str(seconds)], capture_output=True, text=True, env=env, cwd=ROOT)
+    if out.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + out.stderr[-2000:])
+    res = json.loads(out.stdout.strip().splitlines()[-1])
+    res["threads"] = threads
+    return res
+
+
+def cpu_baseline(seconds=12.0):
+    r = run_oracle_sample(seconds)
+    return {"value": round(r["gbs"], 4), "unit": "GB/s", "cores": r["threads"], "kind": "oracle",
+            "sample": f"oracle fp64 GEMV + top-1 on {SAMPLE_ROWS} of the {VOCAB} vocabulary rows "
+                      f"at rows 1/5/10/15, repeated for {r['seconds']:.1f} s ({r['calls']} calls)"}
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"tfd_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------------
+def dist_setup(gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def time_calls(fn, iters, stream):
+    """Mean device time of fn() in ms over iters calls (CUDA events on the launching stream)."""
+    import torch
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def run_ours(args):
+    import torch
+
+    from speculative_decoding_draft_row_gb300 import tfd
+    from synth import inputs
+
+    rank, world, local = dist_setup(args.gpus)
+    stream = torch.cuda.current_stream()
+    w, _ = inputs.head(tie_frac=0.01, seed=rank)
+    wd = w.cuda()
+    del w
+    x_host = inputs.rows(16, seed=rank).pin_memory()
+    xs = {r: x_host[:r].cuda() for r in ROWS}
+    ys = {r: torch.empty((r, VOCAB), dtype=torch.float32, device="cuda") for r in ROWS}
+    tv = {r: torch.empty((r, 1), dtype=torch.float32, device="cuda") for r in ROWS}
+    ti = {r: torch.empty((r, 1), dtype=torch.int32, device="cuda") for r in ROWS}
+    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(16, VOCAB, 1))
+
+    def call(r, x=None):
+        tfd.tfd_head_gemv(wd, tfd.W_BF16, None, xs[r] if x is None else x, tfd.OUT_F32, y=ys[r],
+                          topk=1, top_vals=tv[r], top_ids=ti[r], ws=ws)
+
+    def step():
+        for r in ROWS:
+            call(r)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    # ---- timed region: K steps, one event pair per call ----
+    n = args.steps * len(ROWS)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        evs[0].record(stream)
+        i = 0
+        for _ in range(args.steps):
+            for r in ROWS:
+                call(r)
+                i += 1
+                evs[i].record(stream)
+        evs[-1].synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = evs[0].elapsed_time(evs[-1])
+    per_call = {r: [] for r in ROWS}
+    i = 0
+    for _ in range(args.steps):
+        for r in ROWS:
+            per_call[r].append(evs[i].elapsed_time(evs[i + 1]))
+            i += 1
+    step_bytes = sum(bf16_call_bytes(r) for r in ROWS)
+    ms_step = max_over_ranks(total_ms / args.steps, world)
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+
+    pk = peaks()
+    peak = pk["hbm_gbs"] if pk else 6800.0
+    per_rows = {}
+    kern_ms = 0.0
+    for r in ROWS:
+        us = statistics.median(per_call[r]) * 1e3
+        gbs = bf16_call_bytes(r) / (us * 1e-6) / 1e9
+        per_rows[str(r)] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        kern_ms += statistics.mean(per_call[r])
+    achieved = step_bytes / (kern_ms * 1e-3) / 1e9
+
+    # ---- e2e: the same calls through the public API with host buffers ----
+    top_host = {r: torch.empty((r, 1), dtype=torch.int32).pin_memory() for r in ROWS}
+    val_host = {r: torch.empty((r, 1), dtype=torch.float32).pin_memory() for r in ROWS}
+    xdev = {r: torch.empty((r, HIDDEN), dtype=torch.bfloat16, device="cuda") for r in ROWS}
+
+    def e2e_step():
+        for r in ROWS:
+            xdev[r].copy_(x_host[:r], non_blocking=True)
+            call(r, xdev[r])
+            top_host[r].copy_(ti[r], non_blocking=True)
+            val_host[r].copy_(tv[r], non_blocking=True)
+
+    e2e_steps = max(10, args.steps // 4)
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    e2e_ms = max_over_ranks(time_calls(e2e_step, e2e_steps, stream), world)
+    h2d = sum(r * HIDDEN * 2 for r in ROWS)
+    d2h = sum(r * 8 for r in ROWS)
+
+    # ---- FP8 head, fused top-64 (reported beside the headline) ----
+    fp8 = {}
+    for mode, name in ((tfd.W_FP8_BLOCK32, "e4m3_e8m0_32x32"), (tfd.W_FP8_ROW, "e4m3_row")):
+        codes, scales = tfd.tfd_quant_fp8(wd, mode)
+        ws64 = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(16, VOCAB, 64))
+        out = {}
+        for r in ROWS:
+            v64 = torch.empty((r, 64), dtype=torch.float32, device="cuda")
+            i64 = torch.empty((r, 64), dtype=torch.int32, device="cuda")
+            f = lambda: tfd.tfd_head_gemv(codes, mode, scales, xs[r], tfd.OUT_NONE, topk=64,
+                                          top_vals=v64, top_ids=i64, ws=ws64)
+            for _ in range(3):
+                f()
+            ms = time_calls(f, 20, stream)
+            gbs = fp8_call_bytes(r) / (ms * 1e-3) / 1e9
+            out[str(r)] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                           "frac": round(gbs / peak, 4)}
+        fp8[name] = out
+        del codes, scales
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) head, N(0,1) rows)",
+        "config": {"workload": WORKLOAD, "vocab": VOCAB, "hidden": HIDDEN, "rows": list(ROWS),
+                   "l2": "weights 1.34 GB exceed the 129 MB L2; no flush needed",
+                   "parallelism": f"replicas x{world}"},
+        "per_rows": per_rows,
+        "fp8_top64": fp8,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk else "fallback"},
+        "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": n,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_step = []
+    last = None
+    for i in range(args.warmup + args.steps):
+        r = run_oracle_sample(2.0)
+        if i >= args.warmup:
+            per_step.append(r)
+        last = r
+    gbs = statistics.mean(p["gbs"] for p in per_step)
+    ms = statistics.mean(p["seconds"] for p in per_step) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "vocab": VOCAB, "hidden": HIDDEN,
+                                        "rows": list(ROWS)},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": last["threads"],
+                         "kind": "oracle",
+                         "sample": f"each step: the oracle's fp64 GEMV + top-1 on {SAMPLE_ROWS} of "
+                                   f"{VOCAB} vocabulary rows at rows 1/5/10/15, about 2 s"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    if len(sys.argv) > 2 and sys.argv[1] == "--oracle-worker":
+        oracle_sample_worker(float(sys.argv[2]))
+        return
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

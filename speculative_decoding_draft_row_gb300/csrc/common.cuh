@@ -1,0 +1,124 @@
+// common.cuh - device and host helpers shared by the libtfd kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tfd.h"
+
+namespace tfd {
+
+// ---- ordering keys ------------------------------------------------------------------------------
+// Every top-k here ranks by (value desc, id asc), with -0 == +0 and NaN below -inf. A 64-bit key
+// whose unsigned order is that ranking: high word = order-preserving image of the value (NaN -> 0),
+// low word = complement of the biased id (lower id -> larger word).
+
+__device__ __forceinline__ uint32_t value_key(float v) {
+  if (v != v) return 0u;
+  uint32_t b = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint64_t key) {
+  uint32_t k = (uint32_t)(key >> 32);
+  if (k == 0u) return __uint_as_float(0x7FC00000u);
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__device__ __forceinline__ uint32_t id_key(int32_t id) { return ~((uint32_t)id ^ 0x80000000u); }
+
+__device__ __forceinline__ int32_t key_id(uint64_t key) {
+  return (int32_t)(~(uint32_t)key ^ 0x80000000u);
+}
+
+__device__ __forceinline__ uint64_t make_key(float v, int32_t id) {
+  return ((uint64_t)value_key(v) << 32) | id_key(id);
+}
+
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+  uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+  uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+  return ((uint64_t)hi << 32) | lo;
+}
+
+__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+
+// ---- device status ------------------------------------------------------------------------------
+__device__ __forceinline__ void set_dev_status(int32_t* st, int code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+// ---- bf16 ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+  return __uint_as_float((uint32_t)b << 16);
+}
+
+// ---- streaming loads ----------------------------------------------------------------------------
+// Weights are read once per call: bypass L1 and ask L2 for 256-byte fetches.
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0,%1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p));
+  return v;
+}
+
+// ---- warp reductions ----------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+  return v;
+}
+
+}  // namespace tfd
+
+// ---- host helpers (shared by the C entry points) -----------------------------------------------
+namespace tfd_host {
+
+inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+inline cudaStream_t as_stream(void* s) { return (cudaStream_t)s; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Launch status: the CUDA error of the launch just made, as a tfd_status.
+inline tfd_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TFD_OK : TFD_ERR_CUDA;
+}
+
+// Number of SMs of the current device (0 when no device answers).
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace tfd_host
+
+// Internal launchers shared across translation units.
+namespace tfd_internal {
+// Split top-k over fp32 logits (see topk.cu). The workspace is tfd_topk_workspace() bytes.
+tfd_status topk_launch(const float* logits, int rows, int64_t n, int64_t ld, int k,
+                       const int32_t* id_map, float* vals, int32_t* ids, int64_t ld_out, void* ws,
+                       size_t ws_bytes, cudaStream_t stream);
+size_t topk_workspace(int rows, int64_t n, int k);
+}  // namespace tfd_internal

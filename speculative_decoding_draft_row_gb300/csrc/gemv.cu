@@ -1,0 +1,573 @@
+// gemv.cu - few-row vocabulary-head GEMV (bf16, FP8 row-scaled, FP8 32x32-block-scaled weights)
+// fused with the output modes and a split-vocabulary top-1 (top-k > 1 via topk.cu).
+//
+// Follows the TFE draft head page (#42), commit "pass kernels and FP8 linears": GEMV over bf16 and
+// e4m3 weights for up to 16 rows, out bf16 / fp32 / added to bf16, and the top-1 of a vocabulary
+// row in parts and a join; the DSpark FP8 head page (#3296), "FP8 draft head": E4M3 codes with
+// E8M0 scales in 32x32 blocks, the drafter's top 64 candidates.
+//
+// Design (GB300, HBM-bound): a 1..16-row GEMV reads every weight byte once, so the kernel is a
+// weight stream. Each block is persistent and owns a contiguous range of 64-row groups (one
+// "part" of the vocabulary). Its 16 warps split a group as 4 row tiles x 4 k slices; every warp
+// streams its 16 rows x k-slice straight from HBM into registers with 16-byte (FP8 block form:
+// 8-byte) non-allocating loads kept D steps ahead, and feeds them to warp-level bf16 tensor-core
+// MMAs (m16n8k16, fp32 accumulate) whose other operand is the activation tile held in shared
+// memory in fragment order (conflict-free 16-byte reads). The MMA removes the per-element FMA
+// work that would otherwise cap the CUDA cores at 10-16 rows; FP8 codes are widened to bf16 in
+// registers (exact). The k order inside a dot product is permuted consistently between weights
+// and activations so that each thread's 16 contiguous bytes are one MMA operand chunk.
+// Per group, the four k-slice partials are summed in a fixed order in shared memory, so every
+// output's arithmetic is independent of its index and of the part count.
+#include "common.cuh"
+
+namespace {
+
+using namespace tfd;
+
+constexpr int kThreads = 512;
+constexpr int kWarps = 16;
+constexpr int kGroupRows = 64;  // 4 row tiles of 16
+constexpr int kMaxParts = 1024;
+constexpr int kMaxRowsPad = 16;
+
+template <int WF>
+struct WTraits;
+template <>
+struct WTraits<TFD_W_BF16> {  // 8 bf16 per thread-row load (16 B)
+  static constexpr int E = 8, WORDS = 4, ELEM_BYTES = 2;
+};
+template <>
+struct WTraits<TFD_W_FP8_ROW> {  // 16 codes per thread-row load (16 B)
+  static constexpr int E = 16, WORDS = 4, ELEM_BYTES = 1;
+};
+template <>
+struct WTraits<TFD_W_FP8_BLOCK32> {  // 8 codes (8 B): one step = one 32-wide scale block
+  static constexpr int E = 8, WORDS = 2, ELEM_BYTES = 1;
+};
+
+struct GemvArgs {
+  const void* w;
+  const void* scales;
+  int64_t n, k;
+  const void* x;
+  int64_t ldx;
+  int rows;
+  int out_mode;
+  void* y;
+  int64_t ldy;
+  int topk;
+  const int32_t* id_map;
+  float* logits;  // fp32 logits destination for topk > 1 (may equal y), else null
+  int64_t ld_logits;
+  uint64_t* part_keys;  // [parts][16]
+  uint32_t* counter;
+  float* top_vals;
+  int32_t* top_ids;
+  int64_t ldt;  // row stride of top_vals / top_ids
+  int parts;
+  int64_t ngroups;
+  int ssl;  // steps per k slice
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four E4M3 codes -> two bf16x2 words (codes 0,1 and codes 2,3), exactly. Each code's 7 magnitude
+// bits are placed under a bf16 exponent offset by 120 and the sign kept, which is the code's value
+// times 2^-120 (E4M3 subnormals land on bf16 subnormals); one bf16x2 multiply by 2^120 restores it.
+__device__ __forceinline__ void e4m3x4_to_bf16x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  uint32_t t0 = __byte_perm(v, 0u, 0x1404);  // [0, c0, 0, c1]
+  uint32_t t1 = __byte_perm(v, 0u, 0x3424);  // [0, c2, 0, c3]
+  t0 = (t0 & 0x80008000u) | ((t0 >> 4) & 0x07F007F0u);
+  t1 = (t1 & 0x80008000u) | ((t1 >> 4) & 0x07F007F0u);
+  const uint32_t two120 = 0x7B807B80u;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(t0), "r"(two120));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(t1), "r"(two120));
+}
+
+__device__ __forceinline__ float e8m0_scale(uint32_t byte) {
+  return byte == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(byte << 23);
+}
+
+template <int WF>
+struct WLoad {
+  uint32_t r[2][WTraits<WF>::WORDS];  // rows g and g + 8
+  float sc;                           // block scale (FP8_BLOCK32)
+};
+
+// One bf16 value split into hi + mid + lo bf16 parts (exact for normal fp32 values).
+__device__ __forceinline__ void split3(float v, uint16_t& h0, uint16_t& h1, uint16_t& h2) {
+  h0 = f32_to_bf16_bits(v);
+  float r1 = v - bf16_bits_to_f32(h0);
+  h1 = f32_to_bf16_bits(r1);
+  float r2 = r1 - bf16_bits_to_f32(h1);
+  h2 = f32_to_bf16_bits(r2);
+}
+
+template <int WF, int XF, int NT>
+struct Layout {
+  static constexpr int E = WTraits<WF>::E;
+  static constexpr int H = E / 8;                    // 16-byte x chunks per (step, nt) per lane
+  static constexpr int PL = XF == TFD_X_F32 ? 3 : 1; // activation planes
+  __host__ __device__ static size_t x_bytes(int ssl) { return (size_t)PL * 4 * ssl * NT * H * 32 * 16; }
+  __host__ __device__ static size_t red_bytes() { return (size_t)2 * kWarps * NT * 32 * 16; }
+  __host__ __device__ static size_t best_bytes() { return (size_t)4 * 16 * 8 + 16 * kWarps * 8; }
+  __host__ __device__ static size_t smem_bytes(int ssl) { return x_bytes(ssl) + red_bytes() + best_bytes(); }
+};
+
+template <int WF, int XF, int NT, int D>
+__global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
+  using L = Layout<WF, XF, NT>;
+  using T = WTraits<WF>;
+  constexpr int E = T::E, H = L::H, PL = L::PL, EB = T::ELEM_BYTES;
+  constexpr int MMAJ = E / 4;   // k16 MMAs per step per n-tile
+  constexpr int STEPK = 4 * E;  // k elements per step (4 threads x E)
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int ssl = a.ssl;
+  const int spad = 4 * ssl;
+  uint4* xs = reinterpret_cast<uint4*>(smem);
+  float4* red = reinterpret_cast<float4*>(smem + L::x_bytes(ssl));
+  uint64_t* sbest = reinterpret_cast<uint64_t*>(smem + L::x_bytes(ssl) + L::red_bytes());
+  uint64_t* sjoin = sbest + 64;
+  __shared__ int is_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int mt = warp & 3, ks = warp >> 2;
+  const int64_t K = a.k, N = a.n;
+  const int rows = a.rows;
+
+  if (tid < 64) sbest[tid] = 0ull;
+  // ---- activations -> shared memory, in MMA B-fragment order ----
+  {
+    const int chunks_per_row = spad * STEPK / 8;
+    const int total = 8 * NT * chunks_per_row;
+    for (int idx = tid; idx < total; idx += kThreads) {
+      const int r = idx / chunks_per_row;
+      const int c = idx - r * chunks_per_row;
+      const int k0 = c * 8;
+      const int s = k0 / STEPK;
+      const int rem = k0 - s * STEPK;
+      const int tt = rem / E;
+      const int hf = (rem - tt * E) >> 3;
+      const int ln = (r & 7) * 4 + tt;
+      const int nt = r >> 3;
+      const bool ok = r < rows && k0 < K;
+      if (XF == TFD_X_BF16) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (ok)
+          v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                              (int64_t)r * a.ldx + k0);
+        xs[((s * NT + nt) * H + hf) * 32 + ln] = v;
+      } else {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = 0.0f;
+        if (ok) {
+          const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) +
+                                                            (int64_t)r * a.ldx + k0);
+          float4 u = p[0], w = p[1];
+          f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
+          f[4] = w.x; f[5] = w.y; f[6] = w.z; f[7] = w.w;
+        }
+        uint16_t h[3][8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) split3(f[e], h[0][e], h[1][e], h[2][e]);
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl) {
+          uint4 v;
+          v.x = h[pl][0] | ((uint32_t)h[pl][1] << 16);
+          v.y = h[pl][2] | ((uint32_t)h[pl][3] << 16);
+          v.z = h[pl][4] | ((uint32_t)h[pl][5] << 16);
+          v.w = h[pl][6] | ((uint32_t)h[pl][7] << 16);
+          xs[(((pl * spad + s) * NT + nt) * H + hf) * 32 + ln] = v;
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- weight stream ----
+  const int64_t g_begin = (int64_t)blockIdx.x * a.ngroups / a.parts;
+  const int64_t g_end = (int64_t)(blockIdx.x + 1) * a.ngroups / a.parts;
+  const int s_begin = ks * ssl;
+  const unsigned char* wbase = reinterpret_cast<const unsigned char*>(a.w);
+  const int64_t row_bytes = K * EB;
+  const uint8_t* blk_scales = reinterpret_cast<const uint8_t*>(a.scales);
+  const float* row_scales = reinterpret_cast<const float*>(a.scales);
+  const int64_t kblocks = K >> 5;
+
+  int64_t ld_g = g_begin;
+  int ld_s = 0;
+  auto issue = [&](WLoad<WF>& b) {
+#pragma unroll
+    for (int i = 0; i < T::WORDS; ++i) { b.r[0][i] = 0u; b.r[1][i] = 0u; }
+    b.sc = 0.0f;
+    if (ld_g < g_end) {
+      const int64_t row = ld_g * kGroupRows + mt * 16 + g;
+      const int s = s_begin + ld_s;
+      const int64_t kk = (int64_t)s * STEPK + t * E;
+      if (kk < K) {
+        const unsigned char* p0 = wbase + row * row_bytes + kk * EB;
+        if (WF == TFD_W_FP8_BLOCK32) {
+          if (row < N) { uint2 v = ldg_stream8(p0); b.r[0][0] = v.x; b.r[0][1] = v.y; }
+          if (row + 8 < N) {
+            uint2 v = ldg_stream8(p0 + 8 * row_bytes);
+            b.r[1][0] = v.x; b.r[1][1] = v.y;
+          }
+          const int64_t rblk = (ld_g * kGroupRows + mt * 16) >> 5;
+          if (rblk * 32 < N) b.sc = e8m0_scale(__ldg(blk_scales + rblk * kblocks + s));
+        } else {
+          if (row < N) {
+            uint4 v = ldg_stream16(p0);
+            b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
+          }
+          if (row + 8 < N) {
+            uint4 v = ldg_stream16(p0 + 8 * row_bytes);
+            b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
+          }
+        }
+      }
+      if (++ld_s == ssl) { ld_s = 0; ++ld_g; }
+    }
+  };
+
+  auto compute = [&](const WLoad<WF>& b, int sg, float (&acc)[NT][4]) {
+    uint32_t A[MMAJ][4];
+#pragma unroll
+    for (int j = 0; j < MMAJ; ++j) {
+      if (WF == TFD_W_BF16) {
+        A[j][0] = b.r[0][2 * j]; A[j][1] = b.r[1][2 * j];
+        A[j][2] = b.r[0][2 * j + 1]; A[j][3] = b.r[1][2 * j + 1];
+      } else {
+        uint32_t lo0, hi0, lo1, hi1;
+        e4m3x4_to_bf16x2(b.r[0][j], lo0, hi0);
+        e4m3x4_to_bf16x2(b.r[1][j], lo1, hi1);
+        A[j][0] = lo0; A[j][1] = lo1; A[j][2] = hi0; A[j][3] = hi1;
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float c[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] = (WF == TFD_W_FP8_BLOCK32) ? 0.0f : acc[nt][i];
+#pragma unroll
+      for (int pl = 0; pl < PL; ++pl) {
+        uint32_t xw[4 * H];
+#pragma unroll
+        for (int hf = 0; hf < H; ++hf) {
+          uint4 v = xs[(((pl * spad + sg) * NT + nt) * H + hf) * 32 + lane];
+          xw[4 * hf] = v.x; xw[4 * hf + 1] = v.y; xw[4 * hf + 2] = v.z; xw[4 * hf + 3] = v.w;
+        }
+#pragma unroll
+        for (int j = 0; j < MMAJ; ++j)
+          mma_bf16_16816(c, A[j][0], A[j][1], A[j][2], A[j][3], xw[2 * j], xw[2 * j + 1]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        acc[nt][i] = (WF == TFD_W_FP8_BLOCK32) ? fmaf(b.sc, c[i], acc[nt][i]) : c[i];
+    }
+  };
+
+  // Epilogue of one output value: scale, store, rank.
+  uint64_t best[2] = {0ull, 0ull};
+  auto epi = [&](int64_t row, int act, float v, int slot) {
+    if (row >= N || act >= rows) return;
+    if (WF == TFD_W_FP8_ROW) v *= __ldg(row_scales + row);
+    const int64_t yi = (int64_t)act * a.ldy + row;
+    if (a.out_mode == TFD_OUT_F32) {
+      reinterpret_cast<float*>(a.y)[yi] = v;
+    } else if (a.out_mode == TFD_OUT_BF16) {
+      reinterpret_cast<uint16_t*>(a.y)[yi] = f32_to_bf16_bits(v);
+    } else if (a.out_mode == TFD_OUT_ADD_BF16) {
+      uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + yi;
+      *yp = f32_to_bf16_bits(bf16_bits_to_f32(*yp) + v);
+    }
+    if (a.topk == 1) {
+      const int32_t id = a.id_map ? __ldg(a.id_map + row) : (int32_t)row;
+      best[slot] = umax64(best[slot], make_key(v, id));
+    } else if (a.logits != nullptr && a.logits != a.y) {
+      a.logits[(int64_t)act * a.ld_logits + row] = v;
+    }
+  };
+
+  WLoad<WF> buf[D];
+#pragma unroll
+  for (int i = 0; i < D; ++i) issue(buf[i]);
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+  int rb = 0;
+  const int mr = warp & 3, nr = warp >> 2;  // reducer role of warps < 4 * NT
+  for (int64_t gi = g_begin; gi < g_end; ++gi) {
+    for (int s0 = 0; s0 < ssl; s0 += D) {
+#pragma unroll
+      for (int st = 0; st < D; ++st) {
+        compute(buf[st], s_begin + s0 + st, acc);
+        issue(buf[st]);
+      }
+    }
+    // k-slice partials -> shared memory; fixed-order sum; epilogue.
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      red[((rb * kWarps + warp) * NT + nt) * 32 + lane] =
+          make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+    }
+    __syncthreads();
+    if (warp < 4 * NT) {
+      // warp index = ks * 4 + mt, so the partials of row tile mr are warps mr, 4+mr, 8+mr, 12+mr.
+      float4 v = red[((rb * kWarps + mr) * NT + nr) * 32 + lane];
+#pragma unroll
+      for (int ksi = 1; ksi < 4; ++ksi) {
+        float4 u = red[((rb * kWarps + ksi * 4 + mr) * NT + nr) * 32 + lane];
+        v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+      }
+      const int64_t row_lo = gi * kGroupRows + mr * 16 + g;
+      const int act0 = nr * 8 + 2 * t;
+      epi(row_lo, act0, v.x, 0);
+      epi(row_lo, act0 + 1, v.y, 1);
+      epi(row_lo + 8, act0, v.z, 0);
+      epi(row_lo + 8, act0 + 1, v.w, 1);
+    }
+    rb ^= 1;
+  }
+
+  if (a.topk != 1) return;
+  // ---- top-1: block best per row, then the last block to finish joins the parts ----
+  if (warp < 4 * NT) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint64_t key = best[c];
+      key = umax64(key, shfl_xor_u64(key, 4));
+      key = umax64(key, shfl_xor_u64(key, 8));
+      key = umax64(key, shfl_xor_u64(key, 16));
+      if (g == 0) sbest[mr * 16 + nr * 8 + 2 * t + c] = key;
+    }
+  }
+  __syncthreads();
+  if (tid < kMaxRowsPad) {
+    uint64_t m = umax64(umax64(sbest[tid], sbest[16 + tid]), umax64(sbest[32 + tid], sbest[48 + tid]));
+    a.part_keys[(int64_t)blockIdx.x * kMaxRowsPad + tid] = m;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = (atomicAdd(a.counter, 1u) == (uint32_t)(a.parts - 1));
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  uint64_t m[kMaxRowsPad];
+#pragma unroll
+  for (int r = 0; r < kMaxRowsPad; ++r) m[r] = 0ull;
+  for (int p = tid; p < a.parts; p += kThreads) {
+#pragma unroll
+    for (int r = 0; r < kMaxRowsPad; ++r)
+      if (r < rows) m[r] = umax64(m[r], __ldcg(a.part_keys + (int64_t)p * kMaxRowsPad + r));
+  }
+#pragma unroll
+  for (int r = 0; r < kMaxRowsPad; ++r) {
+    uint64_t key = m[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) key = umax64(key, shfl_xor_u64(key, o));
+    if (lane == 0) sjoin[warp * kMaxRowsPad + r] = key;
+  }
+  __syncthreads();
+  if (tid < rows) {
+    uint64_t key = 0ull;
+    for (int w = 0; w < kWarps; ++w) key = umax64(key, sjoin[w * kMaxRowsPad + tid]);
+    a.top_vals[tid * a.ldt] = key_value(key);
+    a.top_ids[tid * a.ldt] = key_id(key);
+  }
+  if (tid == 0) *a.counter = 0u;  // leave the workspace zeroed
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------------
+constexpr int kDepth = 4;                      // weight loads in flight per warp (steps)
+constexpr size_t kSmemLimit = 232448 - 1024;   // sm_100-class dynamic shared memory, minus slack
+
+template <int WF, int XF, int NT>
+size_t gemv_smem(int64_t k, int* ssl_out) {
+  constexpr int E = WTraits<WF>::E;
+  int64_t steps = (k + 4 * E - 1) / (4 * E);
+  int64_t ssl = (steps + 3) / 4;
+  ssl = (ssl + kDepth - 1) / kDepth * kDepth;
+  if (ssl_out) *ssl_out = (int)ssl;
+  return Layout<WF, XF, NT>::smem_bytes((int)ssl);
+}
+
+template <int WF, int XF, int NT>
+tfd_status gemv_launch_t(GemvArgs a, int parts_req, cudaStream_t stream) {
+  int ssl = 0;
+  size_t smem = gemv_smem<WF, XF, NT>(a.k, &ssl);
+  if (smem > kSmemLimit) return TFD_ERR_UNSUPPORTED;
+  auto kern = gemv_kernel<WF, XF, NT, kDepth>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit) !=
+      cudaSuccess)
+    return TFD_ERR_CUDA;
+  int parts = parts_req;
+  if (parts <= 0) {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess)
+      return TFD_ERR_CUDA;
+    if (occ < 1) occ = 1;
+    int64_t p = (int64_t)tfd_host::sm_count() * occ;
+    if (p > a.ngroups) p = a.ngroups;
+    if (p > kMaxParts) p = kMaxParts;
+    if (p < 1) p = 1;
+    parts = (int)p;
+  }
+  a.parts = parts;
+  a.ssl = ssl;
+  kern<<<parts, kThreads, smem, stream>>>(a);
+  return tfd_host::launch_status();
+}
+
+template <int WF, int XF>
+tfd_status gemv_launch_nt(GemvArgs a, int parts, cudaStream_t s) {
+  return a.rows <= 8 ? gemv_launch_t<WF, XF, 1>(a, parts, s) : gemv_launch_t<WF, XF, 2>(a, parts, s);
+}
+
+template <int WF>
+tfd_status gemv_launch_x(GemvArgs a, int xfmt, int parts, cudaStream_t s) {
+  return xfmt == TFD_X_F32 ? gemv_launch_nt<WF, TFD_X_F32>(a, parts, s)
+                           : gemv_launch_nt<WF, TFD_X_BF16>(a, parts, s);
+}
+
+size_t gemv_smem_any(int wfmt, int xfmt, int rows, int64_t k) {
+  const bool two = rows > 8;
+  const bool f32 = xfmt == TFD_X_F32;
+#define TFD_SMEM(WF)                                                                    \
+  (two ? (f32 ? gemv_smem<WF, TFD_X_F32, 2>(k, nullptr) : gemv_smem<WF, TFD_X_BF16, 2>(k, nullptr)) \
+       : (f32 ? gemv_smem<WF, TFD_X_F32, 1>(k, nullptr) : gemv_smem<WF, TFD_X_BF16, 1>(k, nullptr)))
+  if (wfmt == TFD_W_FP8_ROW) return TFD_SMEM(TFD_W_FP8_ROW);
+  if (wfmt == TFD_W_FP8_BLOCK32) return TFD_SMEM(TFD_W_FP8_BLOCK32);
+  return TFD_SMEM(TFD_W_BF16);
+#undef TFD_SMEM
+}
+
+struct GemvWs {
+  uint32_t* counter;
+  uint64_t* part_keys;
+  float* logits;
+  void* topk_ws;
+  size_t topk_bytes;
+};
+
+// Workspace: [counter | part keys for top-1 | fp32 logits for top-k > 1 | top-k workspace].
+size_t gemv_ws_layout(int rows, int64_t n, int topk, bool logits_in_y, char* base, GemvWs* out) {
+  size_t off = 256;
+  size_t keys = topk == 1 ? tfd_host::round_up((size_t)kMaxParts * kMaxRowsPad * 8, 256) : 0;
+  size_t lg = (topk > 1 && !logits_in_y) ? tfd_host::round_up((size_t)rows * n * 4, 256) : 0;
+  size_t tk = topk > 1 ? tfd_internal::topk_workspace(rows, n, topk) : 0;
+  if (out) {
+    out->counter = reinterpret_cast<uint32_t*>(base);
+    out->part_keys = keys ? reinterpret_cast<uint64_t*>(base + off) : nullptr;
+    out->logits = lg ? reinterpret_cast<float*>(base + off + keys) : nullptr;
+    out->topk_ws = tk ? base + off + keys + lg : nullptr;
+    out->topk_bytes = tk;
+  }
+  if (topk == 0) return 0;
+  return off + keys + lg + tk;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
+  return pa < pb + nb && pb < pa + na;
+}
+
+}  // namespace
+
+extern "C" size_t tfd_head_gemv_workspace(int rows, int64_t n, int topk, int parts) {
+  (void)parts;
+  if (rows < 1 || rows > TFD_MAX_ROWS || n < 1 || topk < 0 || topk > TFD_MAX_TOPK || topk > n)
+    return 0;
+  // The fp32 logits of top-k > 1 are counted in the workspace; a call with F32 output keeps them
+  // in y instead and needs less.
+  return gemv_ws_layout(rows, n, topk, false, nullptr, nullptr);
+}
+
+extern "C" int64_t tfd_head_gemv_max_k(int rows, int xfmt) {
+  if (rows < 1 || rows > TFD_MAX_ROWS || (xfmt != TFD_X_BF16 && xfmt != TFD_X_F32)) return 0;
+  int64_t best = 0;
+  for (int64_t k = 256; k <= (1 << 20); k += 256) {
+    bool ok = true;
+    for (int wf = 0; wf < 3 && ok; ++wf) ok = gemv_smem_any(wf, xfmt, rows, k) <= kSmemLimit;
+    if (!ok) break;
+    best = k;
+  }
+  return best;
+}
+
+extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scales, int64_t n,
+                                    int64_t k, const void* x, int xfmt, int rows, int64_t ldx,
+                                    int out_mode, void* y, int64_t ldy, int topk, int parts,
+                                    const int32_t* id_map, float* top_vals, int32_t* top_ids,
+                                    int64_t ldt, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                    void* stream) {
+  using tfd_host::aligned;
+  (void)dev_status;  // no device-data errors are possible in this call
+  if (!w || !x) return TFD_ERR_INVALID;
+  if (wfmt < TFD_W_BF16 || wfmt > TFD_W_FP8_BLOCK32) return TFD_ERR_INVALID;
+  if (xfmt != TFD_X_BF16 && xfmt != TFD_X_F32) return TFD_ERR_INVALID;
+  if (out_mode < TFD_OUT_NONE || out_mode > TFD_OUT_ADD_BF16) return TFD_ERR_INVALID;
+  if (rows < 1 || rows > TFD_MAX_ROWS) return TFD_ERR_INVALID;
+  if (n < 1 || n > (int64_t)INT32_MAX || k < 16 || k % 16 != 0) return TFD_ERR_INVALID;
+  if (wfmt != TFD_W_BF16 && !w_scales) return TFD_ERR_INVALID;
+  if (wfmt == TFD_W_FP8_BLOCK32 && (n % 32 != 0 || k % 32 != 0)) return TFD_ERR_INVALID;
+  const size_t xb = xfmt == TFD_X_F32 ? 4 : 2;
+  if (ldx < k || ((size_t)ldx * xb) % 16 != 0) return TFD_ERR_INVALID;
+  if (!aligned(w, 16) || !aligned(x, 16)) return TFD_ERR_INVALID;
+  if (w_scales && !aligned(w_scales, 4)) return TFD_ERR_INVALID;
+  if (topk < 0 || topk > TFD_MAX_TOPK || topk > n) return TFD_ERR_INVALID;
+  if (topk > 0 && (!top_vals || !top_ids || !aligned(top_vals, 4) || !aligned(top_ids, 4)))
+    return TFD_ERR_INVALID;
+  if (ldt == 0) ldt = topk;
+  if (topk > 0 && ldt < topk) return TFD_ERR_INVALID;
+  if (parts < 0 || parts > kMaxParts) return TFD_ERR_INVALID;
+  if (id_map && !aligned(id_map, 4)) return TFD_ERR_INVALID;
+  const size_t yb = out_mode == TFD_OUT_F32 ? 4 : 2;
+  if (out_mode != TFD_OUT_NONE) {
+    if (!y || ldy < n || !aligned(y, yb)) return TFD_ERR_INVALID;
+    if (overlaps(x, (size_t)rows * ldx * xb, y, (size_t)rows * ldy * yb)) return TFD_ERR_INVALID;
+  }
+  const bool logits_in_y = out_mode == TFD_OUT_F32;
+  GemvWs wl;
+  size_t need = gemv_ws_layout(rows, n, topk, logits_in_y, reinterpret_cast<char*>(ws), &wl);
+  if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16))) return TFD_ERR_WORKSPACE;
+  if (gemv_smem_any(wfmt, xfmt, rows, k) > kSmemLimit) return TFD_ERR_UNSUPPORTED;
+
+  GemvArgs a{};
+  a.w = w; a.scales = w_scales; a.n = n; a.k = k; a.x = x; a.ldx = ldx; a.rows = rows;
+  a.out_mode = out_mode; a.y = y; a.ldy = ldy; a.topk = topk; a.id_map = id_map;
+  a.logits = nullptr;
+  a.ld_logits = 0;
+  if (topk > 1) {
+    a.logits = logits_in_y ? reinterpret_cast<float*>(y) : wl.logits;
+    a.ld_logits = logits_in_y ? ldy : n;
+  }
+  a.part_keys = wl.part_keys;
+  a.counter = wl.counter;
+  a.top_vals = top_vals;
+  a.top_ids = top_ids;
+  a.ldt = ldt;
+  a.ngroups = (n + kGroupRows - 1) / kGroupRows;
+  cudaStream_t s = tfd_host::as_stream(stream);
+  tfd_status st;
+  if (wfmt == TFD_W_FP8_ROW) st = gemv_launch_x<TFD_W_FP8_ROW>(a, xfmt, parts, s);
+  else if (wfmt == TFD_W_FP8_BLOCK32) st = gemv_launch_x<TFD_W_FP8_BLOCK32>(a, xfmt, parts, s);
+  else st = gemv_launch_x<TFD_W_BF16>(a, xfmt, parts, s);
+  if (st != TFD_OK || topk <= 1) return st;
+  return tfd_internal::topk_launch(a.logits, rows, n, a.ld_logits, topk, id_map, top_vals, top_ids,
+                                   ldt, wl.topk_ws, wl.topk_bytes, s);
+}

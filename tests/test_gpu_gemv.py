@@ -1,0 +1,295 @@
+"""GPU parity of tfd_head_gemv (bf16 / FP8 row / FP8 block weights, every output mode, fused
+top-1 and top-k) against the oracle, on small ragged shapes and on the full 163840 x 4096 head."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import (assert_bf16_close, assert_fp32_close, assert_sorted_keys, assert_topk_valid,
+                     need_gpu, np32, same_bits)
+from oracle import gemv as og
+from oracle.quant import quant_fp8_block32, quant_fp8_row
+from oracle.topk import topk as oracle_topk
+from speculative_decoding_draft_row_gb300 import tfd
+from synth import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def make_case(n, k, rows, wfmt, xf32=False, tid=300, tie_frac=0.0):
+    w = inputs.normal_bf16((n, k), 0.02, tid)
+    if tie_frac:
+        inputs.copy_rows(w, *inputs.tie_rows(n, tie_frac, tensor_id=tid + 5))
+    wn = w.float().numpy()
+    if xf32:
+        x = torch.from_numpy(inputs.normal_f32((rows, k), 1.0, tid + 1))
+    else:
+        x = inputs.normal_bf16((rows, k), 1.0, tid + 1)
+    xn = x.float().numpy()
+    if wfmt == tfd.W_BF16:
+        return dict(w=w.cuda(), scales=None, wo=wn, so=None, x=x.cuda(), xo=xn)
+    if wfmt == tfd.W_FP8_ROW:
+        c, s = quant_fp8_row(wn)
+        return dict(w=torch.from_numpy(c).cuda(), scales=torch.from_numpy(s).cuda(), wo=c, so=s,
+                    x=x.cuda(), xo=xn)
+    c, s = quant_fp8_block32(wn)
+    return dict(w=torch.from_numpy(c).cuda(), scales=torch.from_numpy(s).cuda(), wo=c, so=s,
+                x=x.cuda(), xo=xn)
+
+
+def oracle_acc_S(case, wfmt):
+    acc = og.gemv_acc(case["wo"], case["xo"], wfmt, case["so"])
+    S = og.gemv_abs_scale(case["wo"], case["xo"], wfmt, case["so"])
+    return acc, S
+
+
+SHAPES = [  # (n, k, rows, wfmt, xf32)
+    (4096, 256, 1, tfd.W_BF16, False),        # the tiny draft step
+    (1000, 272, 3, tfd.W_BF16, False),        # ragged n and k
+    (63, 16, 9, tfd.W_BF16, False),
+    (4177, 4096, 16, tfd.W_BF16, False),
+    (2048, 256, 16, tfd.W_BF16, True),        # fp32 activations (low-rank second GEMV)
+    (1000, 272, 5, tfd.W_FP8_ROW, False),
+    (4096, 4096, 4, tfd.W_FP8_ROW, False),    # wo
+    (4096, 11008, 4, tfd.W_FP8_ROW, False),   # w2
+    (4160, 1024, 16, tfd.W_FP8_ROW, False),
+    (2048, 4096, 10, tfd.W_FP8_BLOCK32, False),
+    (96, 96, 1, tfd.W_FP8_BLOCK32, False),
+    (4096, 512, 16, tfd.W_FP8_BLOCK32, True),
+]
+
+
+@pytest.mark.parametrize("n,k,rows,wfmt,xf32", SHAPES)
+def test_f32_logits_and_top1(n, k, rows, wfmt, xf32):
+    need_gpu()
+    case = make_case(n, k, rows, wfmt, xf32)
+    y, tv, ti = tfd.tfd_head_gemv(case["w"], wfmt, case["scales"], case["x"], tfd.OUT_F32, topk=1)
+    torch.cuda.synchronize()
+    acc, S = oracle_acc_S(case, wfmt)
+    yg = np32(y)
+    assert_fp32_close(yg, acc.astype(np.float32), S, "logits")
+    ov, oi = oracle_topk(yg, 1)                    # the fused top-1 is the top-1 of its own logits
+    assert np.array_equal(np32(ti).astype(np.int32), oi) and same_bits(np32(tv), ov)
+    assert_topk_valid(np32(tv), ti.cpu().numpy(), acc, S, 1, what="top-1")
+
+
+@pytest.mark.parametrize("out_mode", [tfd.OUT_BF16, tfd.OUT_ADD_BF16, tfd.OUT_NONE])
+@pytest.mark.parametrize("wfmt", [tfd.W_BF16, tfd.W_FP8_ROW, tfd.W_FP8_BLOCK32])
+def test_output_modes(out_mode, wfmt):
+    need_gpu()
+    n, k, rows = 4096, 4096, 4
+    case = make_case(n, k, rows, wfmt, tid=310)
+    res = inputs.normal_bf16((rows, n), 1.0, 315)
+    y = res.clone().cuda() if out_mode == tfd.OUT_ADD_BF16 else None
+    y, tv, ti = tfd.tfd_head_gemv(case["w"], wfmt, case["scales"], case["x"], out_mode, y=y,
+                                  topk=1)
+    torch.cuda.synchronize()
+    acc, S = oracle_acc_S(case, wfmt)
+    if out_mode == tfd.OUT_BF16:
+        assert_bf16_close(np32(y), og.gemv(case["wo"], case["xo"], wfmt, case["so"], og.OUT_BF16))
+    elif out_mode == tfd.OUT_ADD_BF16:
+        ref = og.gemv(case["wo"], case["xo"], wfmt, case["so"], og.OUT_ADD_BF16,
+                      res=res.float().numpy())
+        assert_bf16_close(np32(y), ref)
+    else:
+        assert y is None
+    assert_topk_valid(np32(tv), ti.cpu().numpy(), acc, S, 1, what="top-1")
+
+
+@pytest.mark.parametrize("wfmt", [tfd.W_BF16, tfd.W_FP8_ROW, tfd.W_FP8_BLOCK32])
+def test_fused_topk_matches_own_logits_and_oracle(wfmt):
+    need_gpu()
+    case = make_case(8192, 4096, 16, wfmt, tid=320, tie_frac=0.01)
+    acc, S = oracle_acc_S(case, wfmt)
+    for k in (8, 64, 512):
+        y, tv, ti = tfd.tfd_head_gemv(case["w"], wfmt, case["scales"], case["x"], tfd.OUT_F32,
+                                      topk=k)
+        _, tv2, ti2 = tfd.tfd_head_gemv(case["w"], wfmt, case["scales"], case["x"], tfd.OUT_NONE,
+                                        topk=k)
+        torch.cuda.synchronize()
+        yg = np32(y)
+        ov, oi = oracle_topk(yg, k)
+        assert np.array_equal(ti.cpu().numpy(), oi) and same_bits(np32(tv), ov)
+        assert np.array_equal(ti2.cpu().numpy(), oi) and same_bits(np32(tv2), ov)
+        assert_sorted_keys(np32(tv), ti.cpu().numpy())
+        assert_topk_valid(np32(tv), ti.cpu().numpy(), acc, S, k, what=f"top-{k}")
+
+
+def test_part_count_does_not_change_results():
+    need_gpu()
+    case = make_case(20480, 4096, 5, tfd.W_BF16, tid=330, tie_frac=0.01)
+    ref = None
+    for parts in (0, 1, 2, 7, 64, 320, 1024):
+        y, tv, ti = tfd.tfd_head_gemv(case["w"], tfd.W_BF16, None, case["x"], tfd.OUT_F32, topk=1,
+                                      parts=parts)
+        torch.cuda.synchronize()
+        got = (np32(y), np32(tv), ti.cpu().numpy())
+        if ref is None:
+            ref = got
+        else:
+            assert same_bits(got[0], ref[0]) and same_bits(got[1], ref[1])
+            assert np.array_equal(got[2], ref[2])
+
+
+@pytest.mark.parametrize("wfmt", [tfd.W_BF16, tfd.W_FP8_ROW, tfd.W_FP8_BLOCK32])
+def test_planted_ties_go_to_the_lower_id(wfmt):
+    """Each activation row's best weight row is copied (with its whole 32-row block, so that every
+    weight form stays identical) into another part of the vocabulary, below or above it: the
+    duplicates must get bit-identical logits and the lower id must win."""
+    need_gpu()
+    n, k, rows = 20480, 4096, 8
+    w = inputs.normal_bf16((n, k), 0.02, 340)
+    x = inputs.normal_bf16((rows, k), 1.0, 341)
+    acc0 = og.gemv_acc(w.float().numpy(), x.float().numpy())
+    for r, src in enumerate(np.argmax(acc0, axis=1)):
+        b = int(src) // 32
+        b2 = (b + n // 64 + 7 * r) % (n // 32)
+        w[b2 * 32:(b2 + 1) * 32] = w[b * 32:(b + 1) * 32].clone()
+    wn = w.float().numpy()
+    if wfmt == tfd.W_BF16:
+        wd, sd, wo, so = w.cuda(), None, wn, None
+    else:
+        c, s = (quant_fp8_row if wfmt == tfd.W_FP8_ROW else quant_fp8_block32)(wn)
+        wd, sd, wo, so = torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda(), c, s
+    y, tv, ti = tfd.tfd_head_gemv(wd, wfmt, sd, x.cuda(), tfd.OUT_F32, topk=1)
+    torch.cuda.synchronize()
+    yg = np32(y)
+    acc = og.gemv_acc(wo, x.float().numpy(), wfmt, so)
+    S = og.gemv_abs_scale(wo, x.float().numpy(), wfmt, so)
+    tied = 0
+    for r in range(rows):
+        top = acc[r].max()
+        best = np.flatnonzero(acc[r] == top)
+        rest = acc[r][acc[r] < top]
+        clear = top - rest.max() > 2e-5 * S[r].max()
+        if len(best) > 1:
+            assert len(set(yg[r, best].view(np.uint32).tolist())) == 1
+            if clear:
+                tied += 1
+                assert ti[r, 0].item() == best.min()
+    assert tied >= rows // 2
+
+
+def test_id_map_reports_mapped_ids_and_breaks_ties_by_them():
+    need_gpu()
+    n, k, rows = 4096, 256, 6
+    case = make_case(n, k, rows, tfd.W_BF16, tid=350)
+    perm = np.random.default_rng([0, 351, 0]).permutation(n).astype(np.int32)
+    wp = case["w"][torch.from_numpy(perm.astype(np.int64)).cuda()]
+    idm = torch.from_numpy(perm).cuda()
+    y1, tv1, ti1 = tfd.tfd_head_gemv(case["w"], tfd.W_BF16, None, case["x"], tfd.OUT_F32, topk=1)
+    y2, tv2, ti2 = tfd.tfd_head_gemv(wp, tfd.W_BF16, None, case["x"], tfd.OUT_F32, topk=1,
+                                     id_map=idm)
+    _, tv3, ti3 = tfd.tfd_head_gemv(wp, tfd.W_BF16, None, case["x"], tfd.OUT_F32, topk=16,
+                                    id_map=idm)
+    torch.cuda.synchronize()
+    assert np.array_equal(ti1.cpu().numpy(), ti2.cpu().numpy()) and same_bits(np32(tv1), np32(tv2))
+    ov, oi = oracle_topk(np32(y2), 16, id_map=perm)
+    assert np.array_equal(ti3.cpu().numpy(), oi) and same_bits(np32(tv3), ov)
+
+
+def test_fp8_decode_is_exact_for_every_code():
+    """One-hot activations pick single columns: y = scale * dec(code), exactly, for all codes
+    (subnormal codes included)."""
+    need_gpu()
+    codes = np.arange(256, dtype=np.uint8)
+    codes[codes == 0x7F] = 0x7E
+    codes[codes == 0xFF] = 0xFE
+    n, k = 256, 64
+    cm = np.zeros((n, k), np.uint8)
+    cm[:, 5] = codes
+    s = np.exp2(np.random.default_rng([0, 360, 0]).integers(-20, 5, n)).astype(np.float32)
+    x = np.zeros((2, k), np.float32)
+    x[0, 5] = 1.0
+    x[1, 5] = -3.0
+    xd = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    y, _, _ = tfd.tfd_head_gemv(torch.from_numpy(cm).cuda(), tfd.W_FP8_ROW, torch.from_numpy(s).cuda(),
+                                xd, tfd.OUT_F32)
+    torch.cuda.synchronize()
+    ref = og.gemv(cm, x, og.W_FP8_ROW, s, og.OUT_F32)
+    assert same_bits(np32(y), ref)
+    sb = np.full((n // 32, k // 32), 120, np.uint8)
+    yb, _, _ = tfd.tfd_head_gemv(torch.from_numpy(cm).cuda(), tfd.W_FP8_BLOCK32,
+                                 torch.from_numpy(sb).cuda(), xd, tfd.OUT_F32)
+    torch.cuda.synchronize()
+    assert same_bits(np32(yb), og.gemv(cm, x, og.W_FP8_BLOCK32, sb, og.OUT_F32))
+
+
+def test_add_bf16_in_place_on_a_strided_output():
+    need_gpu()
+    n, k, rows = 4096, 4096, 4
+    case = make_case(n, k, rows, tfd.W_FP8_ROW, tid=370)
+    big = inputs.normal_bf16((rows, n + 64), 1.0, 371).cuda()
+    y = big[:, 32:32 + n]
+    before = big.clone()
+    tfd.tfd_head_gemv(case["w"], tfd.W_FP8_ROW, case["scales"], case["x"], tfd.OUT_ADD_BF16, y=y)
+    torch.cuda.synchronize()
+    ref = og.gemv(case["wo"], case["xo"], og.W_FP8_ROW, case["so"], og.OUT_ADD_BF16,
+                  res=np32(before[:, 32:32 + n]))
+    assert_bf16_close(np32(y), ref)
+    assert torch.equal(big[:, :32], before[:, :32]) and torch.equal(big[:, 32 + n:],
+                                                                    before[:, 32 + n:])
+
+
+def full_head_oracle(w, x, wfmt=og.W_BF16, scales=None, chunk=16384):
+    """Oracle logits and S of the full head, computed a chunk of rows at a time."""
+    n = w.shape[0]
+    accs, Ss = [], []
+    for a in range(0, n, chunk):
+        b = min(n, a + chunk)
+        if wfmt == og.W_FP8_BLOCK32:
+            sc = scales[a // 32:b // 32]
+        elif wfmt == og.W_FP8_ROW:
+            sc = scales[a:b]
+        else:
+            sc = None
+        wc = w[a:b]
+        accs.append(og.gemv_acc(wc, x, wfmt, sc))
+        Ss.append(og.gemv_abs_scale(wc, x, wfmt, sc))
+    return np.concatenate(accs, axis=1), np.concatenate(Ss, axis=1)
+
+
+@pytest.fixture(scope="module")
+def full_head():
+    need_gpu()
+    w, ties = inputs.head(tie_frac=0.01)
+    return w, w.cuda(), ties
+
+
+@pytest.mark.parametrize("rows", [1, 5, 10, 15, 16])
+def test_full_bf16_head(full_head, rows):
+    need_gpu()
+    w, wd, ties = full_head
+    x = inputs.rows(16)[:rows]
+    y, tv, ti = tfd.tfd_head_gemv(wd, tfd.W_BF16, None, x.cuda(), tfd.OUT_F32, topk=1, parts=64)
+    _, tv2, ti2 = tfd.tfd_head_gemv(wd, tfd.W_BF16, None, x.cuda(), tfd.OUT_F32, topk=1)
+    torch.cuda.synchronize()
+    yg = np32(y)
+    acc, S = full_head_oracle(w.float().numpy(), x.float().numpy())
+    assert_fp32_close(yg, acc.astype(np.float32), S, "full-head logits")
+    ov, oi = oracle_topk(yg, 1)
+    assert np.array_equal(ti.cpu().numpy(), oi) and same_bits(np32(tv), ov)
+    assert np.array_equal(ti2.cpu().numpy(), oi)
+    assert_topk_valid(np32(tv), ti.cpu().numpy(), acc, S, 1, what="full top-1")
+    dst, src = ties
+    assert same_bits(yg[:, dst], yg[:, src])          # planted duplicates: identical logits
+
+
+@pytest.mark.parametrize("mode", [tfd.W_FP8_BLOCK32, tfd.W_FP8_ROW])
+@pytest.mark.parametrize("rows", [1, 15])
+def test_full_fp8_head_top64(full_head, mode, rows):
+    need_gpu()
+    w, wd, _ = full_head
+    codes, scales = tfd.tfd_quant_fp8(wd, mode)
+    x = inputs.rows(16)[:rows]
+    y, tv, ti = tfd.tfd_head_gemv(codes, mode, scales, x.cuda(), tfd.OUT_F32, topk=64)
+    _, tv2, ti2 = tfd.tfd_head_gemv(codes, mode, scales, x.cuda(), tfd.OUT_NONE, topk=64)
+    torch.cuda.synchronize()
+    c = codes.cpu().numpy()
+    s = scales.cpu().numpy()
+    acc, S = full_head_oracle(c, x.float().numpy(), mode, s)
+    yg = np32(y)
+    assert_fp32_close(yg, acc.astype(np.float32), S, "fp8 logits")
+    ov, oi = oracle_topk(yg, 64)
+    assert np.array_equal(ti.cpu().numpy(), oi) and same_bits(np32(tv), ov)
+    assert np.array_equal(ti2.cpu().numpy(), oi) and same_bits(np32(tv2), ov)
+    assert_topk_valid(np32(tv), ti.cpu().numpy(), acc, S, 64, what="fp8 top-64")

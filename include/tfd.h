@@ -132,6 +132,31 @@ tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scales, int64_t 
                          int32_t* dev_status, void* stream);
 
 /*
+ * tfd_head_gemv_noalloc - tfd_head_gemv without a caller workspace, for callers that cannot
+ * allocate device memory: code running while a CUDA graph is captured (cudaMalloc is not allowed
+ * there), serving loops that keep allocator calls off the hot path because cudaMalloc can block or
+ * synchronise the device, and plugins whose host framework owns all device memory.
+ *   The pages have no counterpart of this entry point; it is an addition of this library.
+ *   Same arguments and results as tfd_head_gemv, minus ws/ws_bytes. The scratch is a fixed device
+ *   array of TFD_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that loads it until
+ *   the process exits. A call whose tfd_head_gemv_workspace() size exceeds it returns
+ *   TFD_ERR_WORKSPACE and enqueues nothing (top-1 calls always fit; a top-k > 1 call fits only when
+ *   its fp32 logits and top-k lists do, i.e. for small n).
+ *   The first call on a device looks the array's device address up (once per device, with that
+ *   device current); make that first call before any stream capture. Each call clears the part of
+ *   the array it uses on `stream` before the GEMV (so a call that then fails an argument check has
+ *   already enqueued that clear, which touches only the library's own array). Every call shares
+ *   the one array: calls whose work overlaps on the GPU (other streams, other threads) race and
+ *   must be serialised by the caller. It calls no cudaMalloc, cudaFree or allocating library.
+ */
+#define TFD_NOALLOC_SCRATCH_BYTES 262144
+tfd_status tfd_head_gemv_noalloc(const void* w, int wfmt, const void* w_scales, int64_t n,
+                                 int64_t k, const void* x, int xfmt, int rows, int64_t ldx,
+                                 int out_mode, void* y, int64_t ldy, int topk, int parts,
+                                 const int32_t* id_map, float* top_vals, int32_t* top_ids,
+                                 int64_t ldt, int32_t* dev_status, void* stream);
+
+/*
  * tfd_topk - top-k of given fp32 logits, ties to the lower (mapped) id; values and ids bit-exact.
  *   [TFE] commit "... ocabulary head": "the top cand_k low-rank logits (fp32, a tie at the k-th
  *   value by the lower token id)", cand_k 1 to 512; "the top-1 kernel through an id map".

@@ -29,6 +29,8 @@ SIGNATURES = {
     "tfd_head_gemv_max_k": (_i64, [_i32, _i32]),
     "tfd_head_gemv": (_i32, [_vp, _i32, _vp, _i64, _i64, _vp, _i32, _i32, _i64, _i32, _vp, _i64,
                              _i32, _i32, _vp, _vp, _vp, _i64, _vp, _sz, _vp, _vp]),
+    "tfd_head_gemv_noalloc": (_i32, [_vp, _i32, _vp, _i64, _i64, _vp, _i32, _i32, _i64, _i32,
+                                     _vp, _i64, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp]),
     "tfd_topk_workspace": (_sz, [_i32, _i64, _i32]),
     "tfd_topk": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "tfd_rescore_workspace": (_sz, [_i32, _i32]),
@@ -148,6 +150,34 @@ def tfd_head_gemv(w, wfmt, w_scales, x, out_mode=OUT_F32, y=None, topk=0, parts=
                                  _p(top_ids), ldt, _p(ws), ws_bytes, _p(dev_status),
                                  _stream(stream))
     _check("tfd_head_gemv", st)
+    return y, top_vals, top_ids
+
+
+NOALLOC_SCRATCH_BYTES = 262144
+
+
+def tfd_head_gemv_noalloc(w, wfmt, w_scales, x, out_mode=OUT_F32, y=None, topk=0, parts=0,
+                          id_map=None, top_vals=None, top_ids=None, dev_status=None, stream=None):
+    """tfd_head_gemv on the library's fixed scratch (no workspace argument): for callers that
+    cannot allocate device memory. Outputs must be passed in by such callers; the defaults here
+    allocate them only for convenience. Returns (y, top_vals, top_ids)."""
+    _dev(w, x, y, id_map)
+    n, k = w.shape[0], w.shape[1]
+    rows = x.shape[0]
+    xfmt = X_F32 if x.dtype == torch.float32 else X_BF16
+    if y is None and out_mode != OUT_NONE:
+        dt = torch.float32 if out_mode == OUT_F32 else torch.bfloat16
+        y = torch.empty((rows, n), dtype=dt, device=x.device)
+    if topk > 0 and top_vals is None:
+        top_vals = torch.empty((rows, topk), dtype=torch.float32, device=x.device)
+        top_ids = torch.empty((rows, topk), dtype=torch.int32, device=x.device)
+    ldt = top_ids.stride(0) if topk > 0 else 0
+    st = library().tfd_head_gemv_noalloc(_p(w), wfmt, _p(w_scales), n, k, _p(x), xfmt, rows,
+                                         x.stride(0), out_mode, _p(y),
+                                         y.stride(0) if y is not None else 0, topk, parts,
+                                         _p(id_map), _p(top_vals), _p(top_ids), ldt,
+                                         _p(dev_status), _stream(stream))
+    _check("tfd_head_gemv_noalloc", st)
     return y, top_vals, top_ids
 
 

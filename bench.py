@@ -189,13 +189,20 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """The largest of the ranks' values (every rank gets it)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return t.item()
+
+
+def job_throughput(bytes_per_rank_step, ms_per_step_max, world):
+    """Whole-job GB/s: every rank's bytes over the slowest rank's step time."""
+    return bytes_per_rank_step * world / (ms_per_step_max * 1e-3) / 1e9
 
 
 def time_calls(fn, iters, stream):
@@ -266,7 +273,7 @@ def run_ours(args):
             i += 1
     step_bytes = sum(bf16_call_bytes(r) for r in ROWS)
     ms_step = max_over_ranks(total_ms / args.steps, world)
-    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    value = job_throughput(step_bytes, ms_step, world)
 
     pk = peaks()
     peak = pk["hbm_gbs"] if pk else 6800.0
@@ -326,6 +333,8 @@ def run_ours(args):
         fp8[name] = out
         del codes, scales
 
+    draft_pass = measure_pass(wd, stream)
+
     if rank != 0:
         return
     line = {
@@ -338,6 +347,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "per_rows": per_rows,
         "fp8_top64": fp8,
+        "pass_5x4": draft_pass,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                      "algorithmic_bytes_per_launch": round(step_bytes / len(ROWS)),
@@ -350,6 +360,84 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)
+
+
+PASS_STEPS, PASS_STREAMS, PASS_HEADS, PASS_DIM, PASS_RING, PASS_WINDOW = 5, 4, 32, 128, 528, 511
+HIDDEN_FFN = 11008
+
+
+def pass_bytes(head_bytes):
+    """Algorithmic bytes of one 5-step pass: per step the head, wo and w2 (FP8 codes + row scales)
+    and the window's K and V rows of every stream and head."""
+    wo = HIDDEN * HIDDEN + HIDDEN * 4
+    w2 = HIDDEN * HIDDEN_FFN + HIDDEN * 4
+    kv = PASS_STREAMS * PASS_HEADS * (PASS_WINDOW + 1) * PASS_DIM * 2 * 2
+    return PASS_STEPS * (head_bytes + wo + w2 + kv)
+
+
+def measure_pass(wd, stream, reps=20):
+    """The 5-step x 4-stream draft pass, captured as one CUDA graph; returns ms per pass for the
+    bf16 head and for the FP8 (32x32 block) head."""
+    import torch
+
+    from speculative_decoding_draft_row_gb300 import tfd
+    from speculative_decoding_draft_row_gb300.draft_pass import DraftPass
+    from synth import inputs
+
+    wo_c, wo_s = tfd.tfd_quant_fp8(inputs.linear(HIDDEN, HIDDEN, 40).cuda(), tfd.W_FP8_ROW)
+    w2_c, w2_s = tfd.tfd_quant_fp8(inputs.linear(HIDDEN, HIDDEN_FFN, 41).cuda(), tfd.W_FP8_ROW)
+    kr, vr = inputs.rings(PASS_STREAMS, PASS_RING, PASS_HEADS, PASS_DIM)
+    qkv = [inputs.pass_step_qkv(t, PASS_STREAMS, PASS_HEADS, PASS_DIM) for t in range(PASS_STEPS)]
+    us = [inputs.normal_bf16((PASS_STREAMS, HIDDEN_FFN), 1.0, 50 + t) for t in range(PASS_STEPS)]
+    resid = inputs.normal_bf16((PASS_STREAMS, HIDDEN), 1.0, 60)
+    hc, hs = tfd.tfd_quant_fp8(wd, tfd.W_FP8_BLOCK32)
+    out = {}
+    for name, head, fmt, sc in (("bf16_head", wd, tfd.W_BF16, None),
+                                ("fp8_block32_head", hc, tfd.W_FP8_BLOCK32, hs)):
+        dp = DraftPass(wo_c, wo_s, w2_c, w2_s, head, fmt, sc, kr.clone().cuda(), vr.clone().cuda(),
+                       PASS_WINDOW, PASS_STEPS)
+        dp.load([q for q, _, _ in qkv], [k for _, k, _ in qkv], [v for _, _, v in qkv], us,
+                [511, 511, 511, 511], resid.cuda(), [5] * PASS_STREAMS,
+                torch.zeros((PASS_STREAMS, PASS_STEPS), dtype=torch.int32))
+        dp.capture()
+        for _ in range(3):
+            dp.run()
+        ms = time_calls(dp.run, reps, stream)
+        ms_eager = time_calls(dp.enqueue, reps, stream)
+        nb = pass_bytes(head.numel() * head.element_size() + (655360 if sc is not None else 0))
+        out[name] = {"ms_graph": round(ms, 4), "ms_eager": round(ms_eager, 4),
+                     "gbs": round(nb / (ms * 1e-3) / 1e9, 1), "bytes": nb,
+                     "launches": dp.launches()}
+    return out
+
+
+def run_fp8_case(args):
+    """A small case for profiling: the FP8 head with fused top-64 (no logits) at rows 1/5/10/15,
+    warmup + steps calls of each, one JSON line of us per call."""
+    import torch
+
+    from speculative_decoding_draft_row_gb300 import tfd
+    from synth import inputs
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    mode = tfd.W_FP8_ROW if args.fp8 == "row" else tfd.W_FP8_BLOCK32
+    w, _ = inputs.head(tie_frac=0.01)
+    codes, scales = tfd.tfd_quant_fp8(w.cuda(), mode)
+    xs = {r: inputs.rows(16)[:r].cuda() for r in ROWS}
+    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(16, VOCAB, 64))
+    out = {}
+    for r in ROWS:
+        v = torch.empty((r, 64), dtype=torch.float32, device="cuda")
+        i = torch.empty((r, 64), dtype=torch.int32, device="cuda")
+        f = lambda: tfd.tfd_head_gemv(codes, mode, scales, xs[r], tfd.OUT_NONE, topk=64,
+                                      top_vals=v, top_ids=i, ws=ws)
+        for _ in range(args.warmup):
+            f()
+        ms = time_calls(f, args.steps, stream)
+        out[str(r)] = {"us": round(ms * 1e3, 2),
+                       "gbs": round(fp8_call_bytes(r) / (ms * 1e-3) / 1e9, 1)}
+    print(json.dumps({"case": f"fp8 {args.fp8} top-64", "per_rows": out}), flush=True)
 
 
 def run_reference(args):
@@ -391,6 +479,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", choices=["row", "block32"], default=None,
+                    help="profiling case: only the FP8 head with fused top-64")
     ap.add_argument("--no-extras", action="store_true",
                     help="time the headline calls only (no e2e, FP8 or CPU baseline): a small "
                          "case for profiling")
@@ -399,6 +489,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.fp8:
+        run_fp8_case(args)
     else:
         run_ours(args)
 

@@ -61,19 +61,26 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
 }
 
 // ---- streaming loads ----------------------------------------------------------------------------
-// Weights are read once per call: bypass L1 and ask L2 for 256-byte fetches.
+// Weights are read once per call: bypass L1 and (TFD_L2_PREFETCH=1, the default) ask L2 for
+// 256-byte fetches.
+#ifndef TFD_L2_PREFETCH
+#define TFD_L2_PREFETCH 1
+#endif
+#if TFD_L2_PREFETCH
+#define TFD_LD_STREAM "ld.global.nc.L1::no_allocate.L2::256B"
+#else
+#define TFD_LD_STREAM "ld.global.nc.L1::no_allocate"
+#endif
 __device__ __forceinline__ uint4 ldg_stream16(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile(TFD_LD_STREAM ".v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
 }
 __device__ __forceinline__ uint2 ldg_stream8(const void* p) {
   uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0,%1}, [%2];"
-               : "=r"(v.x), "=r"(v.y)
-               : "l"(p));
+  asm volatile(TFD_LD_STREAM ".v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
 

@@ -22,6 +22,24 @@
 
 namespace {
 
+// Weight loads kept in flight per warp, in steps, for one and two n-tiles (tuning macros).
+#ifndef TFD_GEMV_DEPTH_NT1
+#define TFD_GEMV_DEPTH_NT1 4
+#endif
+#ifndef TFD_GEMV_DEPTH_NT2
+#define TFD_GEMV_DEPTH_NT2 8
+#endif
+// Minimum resident blocks per SM asked of the compiler for one n-tile (2 caps registers at 64).
+#ifndef TFD_GEMV_MINB_NT1
+#define TFD_GEMV_MINB_NT1 1
+#endif
+// The 32x32-block FP8 form loads 8 bytes a row per step (half the others), so it keeps twice the
+// steps in flight to hold the same bytes.
+template <int WF, int NT>
+constexpr int gemv_depth() {
+  return (NT == 1 ? TFD_GEMV_DEPTH_NT1 : TFD_GEMV_DEPTH_NT2) * (WF == TFD_W_FP8_BLOCK32 ? 2 : 1);
+}
+
 using namespace tfd;
 
 constexpr int kThreads = 512;
@@ -79,17 +97,30 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Four E4M3 codes -> two bf16x2 words (codes 0,1 and codes 2,3), exactly. Each code's 7 magnitude
-// bits are placed under a bf16 exponent offset by 120 and the sign kept, which is the code's value
-// times 2^-120 (E4M3 subnormals land on bf16 subnormals); one bf16x2 multiply by 2^120 restores it.
-__device__ __forceinline__ void e4m3x4_to_bf16x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
-  uint32_t t0 = __byte_perm(v, 0u, 0x1404);  // [0, c0, 0, c1]
-  uint32_t t1 = __byte_perm(v, 0u, 0x3424);  // [0, c2, 0, c3]
-  t0 = (t0 & 0x80008000u) | ((t0 >> 4) & 0x07F007F0u);
-  t1 = (t1 & 0x80008000u) | ((t1 >> 4) & 0x07F007F0u);
-  const uint32_t two120 = 0x7B807B80u;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(t0), "r"(two120));
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(t1), "r"(two120));
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four E4M3 codes -> two f16x2 words (codes 0,1 and codes 2,3). Every E4M3 value is an f16 value,
+// so the hardware conversion is exact; one instruction widens two codes.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(v));
+}
+
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float f) {
+  return __half_as_ushort(__float2half_rn(f));
+}
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t b) {
+  return __half2float(__ushort_as_half(b));
 }
 
 __device__ __forceinline__ float e8m0_scale(uint32_t byte) {
@@ -102,13 +133,23 @@ struct WLoad {
   float sc;                           // block scale (FP8_BLOCK32)
 };
 
-// One bf16 value split into hi + mid + lo bf16 parts (exact for normal fp32 values).
+// An fp32 value split into three parts of the MMA operand type (bf16 for bf16 weights, f16 for
+// FP8 weights): hi + mid + lo carries every bit of a normal fp32 value.
+template <bool F16>
 __device__ __forceinline__ void split3(float v, uint16_t& h0, uint16_t& h1, uint16_t& h2) {
-  h0 = f32_to_bf16_bits(v);
-  float r1 = v - bf16_bits_to_f32(h0);
-  h1 = f32_to_bf16_bits(r1);
-  float r2 = r1 - bf16_bits_to_f32(h1);
-  h2 = f32_to_bf16_bits(r2);
+  if (F16) {
+    h0 = f32_to_f16_bits(v);
+    float r1 = v - f16_bits_to_f32(h0);
+    h1 = f32_to_f16_bits(r1);
+    float r2 = r1 - f16_bits_to_f32(h1);
+    h2 = f32_to_f16_bits(r2);
+  } else {
+    h0 = f32_to_bf16_bits(v);
+    float r1 = v - bf16_bits_to_f32(h0);
+    h1 = f32_to_bf16_bits(r1);
+    float r2 = r1 - bf16_bits_to_f32(h1);
+    h2 = f32_to_bf16_bits(r2);
+  }
 }
 
 template <int WF, int XF, int NT>
@@ -118,12 +159,15 @@ struct Layout {
   static constexpr int PL = XF == TFD_X_F32 ? 3 : 1; // activation planes
   __host__ __device__ static size_t x_bytes(int ssl) { return (size_t)PL * 4 * ssl * NT * H * 32 * 16; }
   __host__ __device__ static size_t red_bytes() { return (size_t)2 * kWarps * NT * 32 * 16; }
-  __host__ __device__ static size_t best_bytes() { return (size_t)4 * 16 * 8 + 16 * kWarps * 8; }
+  __host__ __device__ static size_t best_bytes() {
+    return (size_t)4 * 16 * 8 + 16 * kWarps * 8 + 2 * 16 * 4;  // + per-row x max and x scale
+  }
   __host__ __device__ static size_t smem_bytes(int ssl) { return x_bytes(ssl) + red_bytes() + best_bytes(); }
 };
 
 template <int WF, int XF, int NT, int D>
-__global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kThreads, NT == 1 ? TFD_GEMV_MINB_NT1 : 1)
+gemv_kernel(const GemvArgs a) {
   using L = Layout<WF, XF, NT>;
   using T = WTraits<WF>;
   constexpr int E = T::E, H = L::H, PL = L::PL, EB = T::ELEM_BYTES;
@@ -136,7 +180,13 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   float4* red = reinterpret_cast<float4*>(smem + L::x_bytes(ssl));
   uint64_t* sbest = reinterpret_cast<uint64_t*>(smem + L::x_bytes(ssl) + L::red_bytes());
   uint64_t* sjoin = sbest + 64;
+  uint32_t* sxmax = reinterpret_cast<uint32_t*>(sjoin + 16 * kWarps);
+  float* sxscale = reinterpret_cast<float*>(sxmax + 16);
   __shared__ int is_last;
+  // FP8 weights run f16 MMAs: each activation row is scaled by a power of two 2^-e_r into f16 range
+  // (max |x| in [2^14, 2^15)), which keeps every bf16 activation exact down to 2^-32 of the row's
+  // max; the epilogue multiplies by 2^e_r.
+  constexpr bool F16 = WF != TFD_W_BF16;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int mt = warp & 3, ks = warp >> 2;
@@ -144,6 +194,43 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   const int rows = a.rows;
 
   if (tid < 64) sbest[tid] = 0ull;
+  if (tid < 16) sxmax[tid] = 0u;
+  __syncthreads();
+  if (F16) {
+    // per-row max |x| over k (non-negative floats order like their bit patterns)
+    const int chunks = (int)((K + 7) / 8);
+    for (int idx = tid; idx < rows * chunks; idx += kThreads) {
+      const int r = idx / chunks;
+      const int k0 = (idx - r * chunks) * 8;
+      float m = 0.0f;
+      if (XF == TFD_X_BF16) {
+        uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                                  (int64_t)r * a.ldx + k0);
+        uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(u[i])), fabsf(bf16_hi(u[i]))));
+      } else {
+        const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) +
+                                                          (int64_t)r * a.ldx + k0);
+        float4 u = p[0], w = p[1];
+        m = fmaxf(fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))),
+                  fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
+      }
+      atomicMax(&sxmax[r], __float_as_uint(m));
+    }
+    __syncthreads();
+  }
+  if (tid < 16) {
+    int e = 0;
+    const uint32_t ef = (sxmax[tid] >> 23) & 0xFFu;
+    if (F16 && sxmax[tid] != 0u && ef != 0xFFu) {
+      e = (int)ef - 127 - 14;
+      e = e < -110 ? -110 : (e > 110 ? 110 : e);
+    }
+    sxscale[tid] = __uint_as_float((uint32_t)(e + 127) << 23);  // 2^e
+    sxmax[tid] = (uint32_t)(127 - e) << 23;                       // bits of 2^-e
+  }
+  __syncthreads();
   // ---- activations -> shared memory, in MMA B-fragment order ----
   {
     const int chunks_per_row = spad * STEPK / 8;
@@ -159,7 +246,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
       const int ln = (r & 7) * 4 + tt;
       const int nt = r >> 3;
       const bool ok = r < rows && k0 < K;
-      if (XF == TFD_X_BF16) {
+      const float inv = F16 ? __uint_as_float(sxmax[r]) : 1.0f;
+      if (XF == TFD_X_BF16 && !F16) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (ok)
           v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
@@ -170,17 +258,28 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) f[e] = 0.0f;
         if (ok) {
-          const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) +
-                                                            (int64_t)r * a.ldx + k0);
-          float4 u = p[0], w = p[1];
-          f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
-          f[4] = w.x; f[5] = w.y; f[6] = w.z; f[7] = w.w;
+          if (XF == TFD_X_BF16) {
+            uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                                      (int64_t)r * a.ldx + k0);
+            uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { f[2 * i] = bf16_lo(u[i]); f[2 * i + 1] = bf16_hi(u[i]); }
+          } else {
+            const float4* p = reinterpret_cast<const float4*>(
+                reinterpret_cast<const float*>(a.x) + (int64_t)r * a.ldx + k0);
+            float4 u = p[0], w = p[1];
+            f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
+            f[4] = w.x; f[5] = w.y; f[6] = w.z; f[7] = w.w;
+          }
         }
         uint16_t h[3][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) split3(f[e], h[0][e], h[1][e], h[2][e]);
+        for (int e = 0; e < 8; ++e) {
+          if (PL == 1) h[0][e] = f32_to_f16_bits(f[e] * inv);   // bf16 x, FP8 weights
+          else split3<F16>(f[e] * inv, h[0][e], h[1][e], h[2][e]);
+        }
 #pragma unroll
-        for (int pl = 0; pl < 3; ++pl) {
+        for (int pl = 0; pl < PL; ++pl) {
           uint4 v;
           v.x = h[pl][0] | ((uint32_t)h[pl][1] << 16);
           v.y = h[pl][2] | ((uint32_t)h[pl][3] << 16);
@@ -197,6 +296,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   const int64_t g_begin = (int64_t)blockIdx.x * a.ngroups / a.parts;
   const int64_t g_end = (int64_t)(blockIdx.x + 1) * a.ngroups / a.parts;
   const int s_begin = ks * ssl;
+  // The loop runs a multiple of D steps per group so the register ring stays in phase; steps past
+  // the slice's own ssl are empty (no loads, zero weights).
+  const int ssl_loop = (ssl + D - 1) / D * D;
   const unsigned char* wbase = reinterpret_cast<const unsigned char*>(a.w);
   const int64_t row_bytes = K * EB;
   const uint8_t* blk_scales = reinterpret_cast<const uint8_t*>(a.scales);
@@ -213,7 +315,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
       const int64_t row = ld_g * kGroupRows + mt * 16 + g;
       const int s = s_begin + ld_s;
       const int64_t kk = (int64_t)s * STEPK + t * E;
-      if (kk < K) {
+      if (ld_s < ssl && kk < K) {
         const unsigned char* p0 = wbase + row * row_bytes + kk * EB;
         if (WF == TFD_W_FP8_BLOCK32) {
           if (row < N) { uint2 v = ldg_stream8(p0); b.r[0][0] = v.x; b.r[0][1] = v.y; }
@@ -234,51 +336,58 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
           }
         }
       }
-      if (++ld_s == ssl) { ld_s = 0; ++ld_g; }
+      if (++ld_s == ssl_loop) { ld_s = 0; ++ld_g; }
     }
   };
 
+  // One step: MMA j of the step takes elements [4j, 4j + 4) of each thread's chunk. All activation
+  // fragments of the step are read first; each weight fragment is widened just before its MMAs.
   auto compute = [&](const WLoad<WF>& b, int sg, float (&acc)[NT][4]) {
-    uint32_t A[MMAJ][4];
+    uint32_t xw[NT][PL][4 * H];
 #pragma unroll
-    for (int j = 0; j < MMAJ; ++j) {
-      if (WF == TFD_W_BF16) {
-        A[j][0] = b.r[0][2 * j]; A[j][1] = b.r[1][2 * j];
-        A[j][2] = b.r[0][2 * j + 1]; A[j][3] = b.r[1][2 * j + 1];
-      } else {
-        uint32_t lo0, hi0, lo1, hi1;
-        e4m3x4_to_bf16x2(b.r[0][j], lo0, hi0);
-        e4m3x4_to_bf16x2(b.r[1][j], lo1, hi1);
-        A[j][0] = lo0; A[j][1] = lo1; A[j][2] = hi0; A[j][3] = hi1;
-      }
-    }
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float c[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) c[i] = (WF == TFD_W_FP8_BLOCK32) ? 0.0f : acc[nt][i];
-#pragma unroll
-      for (int pl = 0; pl < PL; ++pl) {
-        uint32_t xw[4 * H];
+      for (int pl = 0; pl < PL; ++pl)
 #pragma unroll
         for (int hf = 0; hf < H; ++hf) {
           uint4 v = xs[(((pl * spad + sg) * NT + nt) * H + hf) * 32 + lane];
-          xw[4 * hf] = v.x; xw[4 * hf + 1] = v.y; xw[4 * hf + 2] = v.z; xw[4 * hf + 3] = v.w;
+          xw[nt][pl][4 * hf] = v.x; xw[nt][pl][4 * hf + 1] = v.y;
+          xw[nt][pl][4 * hf + 2] = v.z; xw[nt][pl][4 * hf + 3] = v.w;
         }
+    float c[NT][4];
 #pragma unroll
-        for (int j = 0; j < MMAJ; ++j)
-          mma_bf16_16816(c, A[j][0], A[j][1], A[j][2], A[j][3], xw[2 * j], xw[2 * j + 1]);
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[nt][i] = (WF == TFD_W_FP8_BLOCK32) ? 0.0f : acc[nt][i];
+#pragma unroll
+    for (int j = 0; j < MMAJ; ++j) {
+      uint32_t A0, A1, A2, A3;
+      if (WF == TFD_W_BF16) {
+        A0 = b.r[0][2 * j]; A1 = b.r[1][2 * j]; A2 = b.r[0][2 * j + 1]; A3 = b.r[1][2 * j + 1];
+      } else {
+        e4m3x4_to_f16x2(b.r[0][j], A0, A2);
+        e4m3x4_to_f16x2(b.r[1][j], A1, A3);
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        acc[nt][i] = (WF == TFD_W_FP8_BLOCK32) ? fmaf(b.sc, c[i], acc[nt][i]) : c[i];
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int pl = 0; pl < PL; ++pl) {
+          if (F16) mma_f16_16816(c[nt], A0, A1, A2, A3, xw[nt][pl][2 * j], xw[nt][pl][2 * j + 1]);
+          else mma_bf16_16816(c[nt], A0, A1, A2, A3, xw[nt][pl][2 * j], xw[nt][pl][2 * j + 1]);
+        }
     }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        acc[nt][i] = (WF == TFD_W_FP8_BLOCK32) ? fmaf(b.sc, c[nt][i], acc[nt][i]) : c[nt][i];
   };
 
   // Epilogue of one output value: scale, store, rank.
   uint64_t best[2] = {0ull, 0ull};
   auto epi = [&](int64_t row, int act, float v, int slot) {
     if (row >= N || act >= rows) return;
+    if (F16) v *= sxscale[act];
     if (WF == TFD_W_FP8_ROW) v *= __ldg(row_scales + row);
     const int64_t yi = (int64_t)act * a.ldy + row;
     if (a.out_mode == TFD_OUT_F32) {
@@ -308,10 +417,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   int rb = 0;
   const int mr = warp & 3, nr = warp >> 2;  // reducer role of warps < 4 * NT
   for (int64_t gi = g_begin; gi < g_end; ++gi) {
-    for (int s0 = 0; s0 < ssl; s0 += D) {
+    for (int s0 = 0; s0 < ssl_loop; s0 += D) {
 #pragma unroll
       for (int st = 0; st < D; ++st) {
-        compute(buf[st], s_begin + s0 + st, acc);
+        // an empty step (past ssl) reads any valid activation slot: its weights are zero
+        compute(buf[st], s_begin + (s0 + st < ssl ? s0 + st : 0), acc);
         issue(buf[st]);
       }
     }
@@ -393,7 +503,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
 // ---------------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------------
-constexpr int kDepth = 4;                      // weight loads in flight per warp (steps)
+
 constexpr size_t kSmemLimit = 232448 - 1024;   // sm_100-class dynamic shared memory, minus slack
 
 template <int WF, int XF, int NT>
@@ -401,7 +511,6 @@ size_t gemv_smem(int64_t k, int* ssl_out) {
   constexpr int E = WTraits<WF>::E;
   int64_t steps = (k + 4 * E - 1) / (4 * E);
   int64_t ssl = (steps + 3) / 4;
-  ssl = (ssl + kDepth - 1) / kDepth * kDepth;
   if (ssl_out) *ssl_out = (int)ssl;
   return Layout<WF, XF, NT>::smem_bytes((int)ssl);
 }
@@ -411,7 +520,7 @@ tfd_status gemv_launch_t(GemvArgs a, int parts_req, cudaStream_t stream) {
   int ssl = 0;
   size_t smem = gemv_smem<WF, XF, NT>(a.k, &ssl);
   if (smem > kSmemLimit) return TFD_ERR_UNSUPPORTED;
-  auto kern = gemv_kernel<WF, XF, NT, kDepth>;
+  auto kern = gemv_kernel<WF, XF, NT, gemv_depth<WF, NT>()>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit) !=
       cudaSuccess)
     return TFD_ERR_CUDA;

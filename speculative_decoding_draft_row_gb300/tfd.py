@@ -51,10 +51,13 @@ class TfdError(RuntimeError):
 
 
 def library(build=True):
-    """The loaded libtfd.so (built first when missing or stale)."""
+    """The loaded libtfd.so (built first when missing or stale). The environment variable
+    TFD_LIBRARY names another build of the library to load instead (it must exist)."""
     global _lib
     if _lib is None:
-        path = _build.build_library() if build else _build.LIB_PATH
+        path = os.environ.get("TFD_LIBRARY")
+        if not path:
+            path = _build.build_library() if build else _build.LIB_PATH
         if not os.path.exists(path):
             raise RuntimeError(f"libtfd.so not found at {path}")
         lib = ctypes.CDLL(path)

@@ -10,6 +10,7 @@ Tensor ids (one per role, so every tensor has its own stream):
   10+3t / 11+3t / 12+3t q, k, v of pass step t, 30 / 31 prefilled K / V rings,
   40 wo, 41 w2, 50+t w2 input of step t, 60 residual, 70 draws, 80+ test-only tensors.
 """
+import functools
 from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
@@ -70,7 +71,15 @@ def copy_rows(w, dst, src):
 # --- workload builders ------------------------------------------------------------------------
 
 def head(vocab=163840, hidden=4096, std=0.02, tie_frac=0.0, seed=0):
-    """Vocabulary head W [vocab][hidden] bf16 (tensor 1), with optional planted duplicate rows."""
+    """Vocabulary head W [vocab][hidden] bf16 (tensor 1), with optional planted duplicate rows.
+
+    The result is cached per process (the full head takes seconds to draw): callers must not modify
+    it in place."""
+    return _head(vocab, hidden, std, tie_frac, seed)
+
+
+@functools.lru_cache(maxsize=2)
+def _head(vocab, hidden, std, tie_frac, seed):
     w = normal_bf16((vocab, hidden), std, 1, seed)
     ties = None
     if tie_frac > 0:

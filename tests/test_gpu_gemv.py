@@ -189,25 +189,27 @@ def test_id_map_reports_mapped_ids_and_breaks_ties_by_them():
 
 def test_fp8_decode_is_exact_for_every_code():
     """One-hot activations pick single columns: y = scale * dec(code), exactly, for all codes
-    (subnormal codes included)."""
+    (subnormal codes included) and for every byte position within a 16-byte weight chunk."""
     need_gpu()
     codes = np.arange(256, dtype=np.uint8)
     codes[codes == 0x7F] = 0x7E
     codes[codes == 0xFF] = 0xFE
-    n, k = 256, 64
+    n, k, rows = 256, 64, 16
     cm = np.zeros((n, k), np.uint8)
-    cm[:, 5] = codes
+    for c in range(rows):
+        cm[:, c] = np.roll(codes, 17 * c)
     s = np.exp2(np.random.default_rng([0, 360, 0]).integers(-20, 5, n)).astype(np.float32)
-    x = np.zeros((2, k), np.float32)
-    x[0, 5] = 1.0
-    x[1, 5] = -3.0
+    x = np.zeros((rows, k), np.float32)
+    for r in range(rows):
+        x[r, r] = (-1.0) ** r * 2.0 ** (r - 6)
     xd = torch.from_numpy(x).to(torch.bfloat16).cuda()
-    y, _, _ = tfd.tfd_head_gemv(torch.from_numpy(cm).cuda(), tfd.W_FP8_ROW, torch.from_numpy(s).cuda(),
-                                xd, tfd.OUT_F32)
+    y, _, _ = tfd.tfd_head_gemv(torch.from_numpy(cm).cuda(), tfd.W_FP8_ROW,
+                                torch.from_numpy(s).cuda(), xd, tfd.OUT_F32)
     torch.cuda.synchronize()
-    ref = og.gemv(cm, x, og.W_FP8_ROW, s, og.OUT_F32)
-    assert same_bits(np32(y), ref)
+    assert same_bits(np32(y), og.gemv(cm, x, og.W_FP8_ROW, s, og.OUT_F32))
     sb = np.full((n // 32, k // 32), 120, np.uint8)
+    sb[3, 0] = 0
+    sb[5, 1] = 200
     yb, _, _ = tfd.tfd_head_gemv(torch.from_numpy(cm).cuda(), tfd.W_FP8_BLOCK32,
                                  torch.from_numpy(sb).cuda(), xd, tfd.OUT_F32)
     torch.cuda.synchronize()

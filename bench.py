@@ -334,6 +334,7 @@ def run_ours(args):
         del codes, scales
 
     draft_pass = measure_pass(wd, stream)
+    path_rows = measure_rows_of_path(wd, stream, peak)
 
     if rank != 0:
         return
@@ -348,6 +349,7 @@ def run_ours(args):
         "per_rows": per_rows,
         "fp8_top64": fp8,
         "pass_5x4": draft_pass,
+        "rows_of_path": path_rows,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                      "algorithmic_bytes_per_launch": round(step_bytes / len(ROWS)),
@@ -411,6 +413,73 @@ def measure_pass(wd, stream, reps=20):
     return out
 
 
+def measure_rows_of_path(wd, stream, peak):
+    """The other rows of the step, each timed alone (CUDA events, mean over repetitions) and
+    reported as us per call and algorithmic GB/s against the HBM peak."""
+    import torch
+
+    from speculative_decoding_draft_row_gb300 import tfd
+    from synth import inputs
+
+    out = {}
+
+    def rec(name, fn, nbytes, reps=20):
+        for _ in range(3):
+            fn()
+        ms = time_calls(fn, reps, stream)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "bytes": nbytes}
+
+    # two-stage head, 16 rows: B x, A h, top cand_k of the low-rank logits, exact rescore
+    a, b = inputs.low_rank()
+    ad, bd = a.cuda(), b.cuda()
+    x16 = inputs.rows(16).cuda()
+    h = torch.empty((16, 256), dtype=torch.float32, device="cuda")
+    z = torch.empty((16, VOCAB), dtype=torch.float32, device="cuda")
+    for ck in (1, 64, 512):
+        cv = torch.empty((16, ck), dtype=torch.float32, device="cuda")
+        ci = torch.empty((16, ck), dtype=torch.int32, device="cuda")
+        tws = tfd.zeroed_workspace(tfd.tfd_topk_workspace(16, VOCAB, ck))
+        rws = tfd.zeroed_workspace(tfd.tfd_rescore_workspace(16, ck))
+        oi = torch.empty(16, dtype=torch.int32, device="cuda")
+        ov = torch.empty(16, dtype=torch.float32, device="cuda")
+
+        def two_stage():
+            tfd.tfd_head_gemv(bd, tfd.W_BF16, None, x16, tfd.OUT_F32, y=h)
+            tfd.tfd_head_gemv(ad, tfd.W_BF16, None, h, tfd.OUT_F32, y=z)
+            tfd.tfd_topk(z, ck, vals=cv, ids=ci, ws=tws)
+            tfd.tfd_rescore(wd, x16, ci, out_ids=oi, out_vals=ov, ws=rws, want_logits=False)
+
+        # what the method must move: B, A, the activations and the gathered exact-head rows
+        nbytes = 256 * HIDDEN * 2 + VOCAB * 256 * 2 + 16 * HIDDEN * 2 + 16 * ck * HIDDEN * 2
+        rec(f"two_stage_cand{ck}", two_stage, nbytes)
+    del ad, bd
+    # window attention of one pass step: 4 streams x 32 heads, window 511 (512 keys)
+    kr, vr = inputs.rings(PASS_STREAMS, PASS_RING, PASS_HEADS, PASS_DIM)
+    krd, vrd = kr.cuda(), vr.cuda()
+    q, k, v = (t.cuda() for t in inputs.pass_step_qkv(0))
+    pos = torch.full((PASS_STREAMS,), 511, dtype=torch.int32, device="cuda")
+    att = torch.empty((PASS_STREAMS, PASS_HEADS * PASS_DIM), dtype=torch.bfloat16, device="cuda")
+    rec("window_attn_4x32_w511",
+        lambda: tfd.tfd_window_attn(q, k, v, pos, krd, vrd, PASS_WINDOW, out=att),
+        PASS_STREAMS * PASS_HEADS * (PASS_WINDOW + 1) * PASS_DIM * 2 * 2)
+    # accept of a 5-draft window over 4 streams
+    dr = torch.arange(20, dtype=torch.int32, device="cuda").reshape(4, 5)
+    na = torch.full((4,), 5, dtype=torch.int32, device="cuda")
+    nk = torch.empty(4, dtype=torch.int32, device="cuda")
+    rec("accept_4x5", lambda: tfd.tfd_accept(dr, na, dr, n_kept=nk), 4 * 5 * 4 * 2 + 4 * 8)
+    # FP8 quantisation of the head (offline step): bf16 in, codes + scales out
+    for mode, name in ((tfd.W_FP8_ROW, "quant_row_head"), (tfd.W_FP8_BLOCK32, "quant_block32_head")):
+        codes = torch.empty((VOCAB, HIDDEN), dtype=torch.uint8, device="cuda")
+        sc = (torch.empty(VOCAB, dtype=torch.float32, device="cuda") if mode == tfd.W_FP8_ROW
+              else torch.empty((VOCAB // 32, HIDDEN // 32), dtype=torch.uint8, device="cuda"))
+        rec(name, lambda: tfd.tfd_quant_fp8(wd, mode, codes=codes, scales=sc),
+            VOCAB * HIDDEN * 3 + sc.numel() * sc.element_size(), reps=5)
+        del codes, sc
+    return out
+
+
 def run_fp8_case(args):
     """A small case for profiling: the FP8 head with fused top-64 (no logits) at rows 1/5/10/15,
     warmup + steps calls of each, one JSON line of us per call."""
@@ -438,6 +507,67 @@ def run_fp8_case(args):
         out[str(r)] = {"us": round(ms * 1e3, 2),
                        "gbs": round(fp8_call_bytes(r) / (ms * 1e-3) / 1e9, 1)}
     print(json.dumps({"case": f"fp8 {args.fp8} top-64", "per_rows": out}), flush=True)
+
+
+def run_case(args):
+    """Small isolated cases for profiling: one call of one row of the path, repeated."""
+    import torch
+
+    from speculative_decoding_draft_row_gb300 import tfd
+    from synth import inputs
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    c = args.case
+    if c == "attn":
+        kr, vr = inputs.rings(PASS_STREAMS, PASS_RING, PASS_HEADS, PASS_DIM)
+        krd, vrd = kr.cuda(), vr.cuda()
+        q, k, v = (t.cuda() for t in inputs.pass_step_qkv(0))
+        pos = torch.full((PASS_STREAMS,), 511, dtype=torch.int32, device="cuda")
+        out = torch.empty((PASS_STREAMS, PASS_HEADS * PASS_DIM), dtype=torch.bfloat16,
+                          device="cuda")
+        fn = lambda: tfd.tfd_window_attn(q, k, v, pos, krd, vrd, PASS_WINDOW, out=out)
+    elif c in ("rescore", "topk512", "twostage"):
+        x16 = inputs.rows(16).cuda()
+        if c == "topk512":
+            z = torch.from_numpy(inputs.normal_f32((16, VOCAB), 1.0, 90)).cuda()
+            ws = tfd.zeroed_workspace(tfd.tfd_topk_workspace(16, VOCAB, 512))
+            cv = torch.empty((16, 512), dtype=torch.float32, device="cuda")
+            ci = torch.empty((16, 512), dtype=torch.int32, device="cuda")
+            fn = lambda: tfd.tfd_topk(z, 512, vals=cv, ids=ci, ws=ws)
+        else:
+            w, _ = inputs.head(tie_frac=0.01)
+            wd = w.cuda()
+            cand = torch.from_numpy(
+                __import__("numpy").random.default_rng([0, 91, 0]).integers(
+                    0, VOCAB, size=(16, 512)).astype("int32")).cuda()
+            rws = tfd.zeroed_workspace(tfd.tfd_rescore_workspace(16, 512))
+            oi = torch.empty(16, dtype=torch.int32, device="cuda")
+            ov = torch.empty(16, dtype=torch.float32, device="cuda")
+            if c == "rescore":
+                fn = lambda: tfd.tfd_rescore(wd, x16, cand, out_ids=oi, out_vals=ov, ws=rws,
+                                             want_logits=False)
+            else:
+                a, b = inputs.low_rank()
+                ad, bd = a.cuda(), b.cuda()
+                h = torch.empty((16, 256), dtype=torch.float32, device="cuda")
+                z = torch.empty((16, VOCAB), dtype=torch.float32, device="cuda")
+                tws = tfd.zeroed_workspace(tfd.tfd_topk_workspace(16, VOCAB, 512))
+                cv = torch.empty((16, 512), dtype=torch.float32, device="cuda")
+                ci = torch.empty((16, 512), dtype=torch.int32, device="cuda")
+
+                def fn():
+                    tfd.tfd_head_gemv(bd, tfd.W_BF16, None, x16, tfd.OUT_F32, y=h)
+                    tfd.tfd_head_gemv(ad, tfd.W_BF16, None, h, tfd.OUT_F32, y=z)
+                    tfd.tfd_topk(z, 512, vals=cv, ids=ci, ws=tws)
+                    tfd.tfd_rescore(wd, x16, ci, out_ids=oi, out_vals=ov, ws=rws,
+                                    want_logits=False)
+    else:
+        raise SystemExit(f"unknown case {c}")
+    for _ in range(args.warmup):
+        fn()
+    ms = time_calls(fn, args.steps, stream)
+    print(json.dumps({"case": c, "us": round(ms * 1e3, 2)}), flush=True)
 
 
 def run_reference(args):
@@ -481,6 +611,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", choices=["row", "block32"], default=None,
                     help="profiling case: only the FP8 head with fused top-64")
+    ap.add_argument("--case", choices=["attn", "rescore", "topk512", "twostage"], default=None,
+                    help="profiling case: one row of the path alone")
     ap.add_argument("--no-extras", action="store_true",
                     help="time the headline calls only (no e2e, FP8 or CPU baseline): a small "
                          "case for profiling")
@@ -491,6 +623,8 @@ def main():
         run_reference(args)
     elif args.fp8:
         run_fp8_case(args)
+    elif args.case:
+        run_case(args)
     else:
         run_ours(args)
 

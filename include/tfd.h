@@ -114,6 +114,10 @@ tfd_status tfd_quant_fp8(const void* w_bf16, int64_t n, int64_t k, int mode, uin
  *            each row's fp32 acc (the FP8_ROW scale and BLOCK32 scales applied).
  *   ldt      row stride of top_vals/top_ids (0 = topk; else >= topk), so that the top-1 of each
  *            step of a multi-step pass can land in one column of a [streams][steps] array.
+ *   top1_conf device float [rows] or NULL; only with topk == 1: the top-1 "with confidence"
+ *            ([TFE] "What this changes": row kernels ... top-1 with confidence), read as the
+ *            softmax probability of the pick, 1 / sum_i exp(acc_i - max acc) over the row's n
+ *            outputs (NaN and -inf outputs add nothing; a row of only those gives NaN).
  *   parts    the row is scanned in `parts` contiguous ranges whose partial top-k are then joined;
  *            0 = the library's choice. The result does not depend on it.
  *   id_map   device int32 [n] or NULL: the id reported (and compared on ties) for output i is
@@ -128,8 +132,8 @@ int64_t tfd_head_gemv_max_k(int rows, int xfmt);
 tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scales, int64_t n, int64_t k,
                          const void* x, int xfmt, int rows, int64_t ldx, int out_mode, void* y,
                          int64_t ldy, int topk, int parts, const int32_t* id_map, float* top_vals,
-                         int32_t* top_ids, int64_t ldt, void* ws, size_t ws_bytes,
-                         int32_t* dev_status, void* stream);
+                         int32_t* top_ids, int64_t ldt, float* top1_conf, void* ws,
+                         size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /*
  * tfd_head_gemv_noalloc - tfd_head_gemv without a caller workspace, for callers that cannot
@@ -149,12 +153,13 @@ tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scales, int64_t 
  *   the one array: calls whose work overlaps on the GPU (other streams, other threads) race and
  *   must be serialised by the caller. It calls no cudaMalloc, cudaFree or allocating library.
  */
-#define TFD_NOALLOC_SCRATCH_BYTES 262144
+#define TFD_NOALLOC_SCRATCH_BYTES 524288
 tfd_status tfd_head_gemv_noalloc(const void* w, int wfmt, const void* w_scales, int64_t n,
                                  int64_t k, const void* x, int xfmt, int rows, int64_t ldx,
                                  int out_mode, void* y, int64_t ldy, int topk, int parts,
                                  const int32_t* id_map, float* top_vals, int32_t* top_ids,
-                                 int64_t ldt, int32_t* dev_status, void* stream);
+                                 int64_t ldt, float* top1_conf, int32_t* dev_status,
+                                 void* stream);
 
 /*
  * tfd_topk - top-k of given fp32 logits, ties to the lower (mapped) id; values and ids bit-exact.

@@ -75,3 +75,19 @@ def topk_parts(logits, k, parts, id_map=None):
         vals[r] = canonical(cv[o])
         ids[r] = ci[o]
     return vals, ids
+
+
+def top1_confidence(logits):
+    """Softmax probability of each row's top-1: ``1 / sum_i exp(l_i - max l)``.
+
+    Follows the TFE draft head page (#42), "What this changes": the row kernels include a "top-1
+    with confidence". Reading: the confidence is the softmax probability of the picked logit over
+    the whole row; NaN and -inf logits add nothing; a row with no other value gives NaN.
+    Computed in float64 from the given logits.
+    """
+    lg = np.atleast_2d(np.asarray(logits, dtype=np.float64))
+    out = np.empty(lg.shape[0], dtype=np.float64)
+    for r, row in enumerate(lg):
+        fin = row[~np.isnan(row) & (row > -np.inf)]
+        out[r] = np.nan if fin.size == 0 else 1.0 / np.sum(np.exp(fin - fin.max()))
+    return out

@@ -22,22 +22,32 @@
 
 namespace {
 
-// Weight loads kept in flight per warp, in steps, for one and two n-tiles (tuning macros).
+// Weight loads kept in flight per warp, in steps, for one and two n-tiles (tuning macros); the
+// FP8 forms have their own two-n-tile depth (their decode needs more registers).
 #ifndef TFD_GEMV_DEPTH_NT1
 #define TFD_GEMV_DEPTH_NT1 4
 #endif
 #ifndef TFD_GEMV_DEPTH_NT2
 #define TFD_GEMV_DEPTH_NT2 8
 #endif
+#ifndef TFD_GEMV_DEPTH_FP8_NT1
+#define TFD_GEMV_DEPTH_FP8_NT1 4
+#endif
+#ifndef TFD_GEMV_DEPTH_FP8_NT2
+#define TFD_GEMV_DEPTH_FP8_NT2 8
+#endif
+#ifndef TFD_GEMV_DEPTH_BLK_NT2
+#define TFD_GEMV_DEPTH_BLK_NT2 8
+#endif
 // Minimum resident blocks per SM asked of the compiler for one n-tile (2 caps registers at 64).
 #ifndef TFD_GEMV_MINB_NT1
 #define TFD_GEMV_MINB_NT1 1
 #endif
-// The 32x32-block FP8 form loads 8 bytes a row per step (half the others), so it keeps twice the
-// steps in flight to hold the same bytes.
 template <int WF, int NT>
 constexpr int gemv_depth() {
-  return (NT == 1 ? TFD_GEMV_DEPTH_NT1 : TFD_GEMV_DEPTH_NT2) * (WF == TFD_W_FP8_BLOCK32 ? 2 : 1);
+  return WF == TFD_W_BF16 ? (NT == 1 ? TFD_GEMV_DEPTH_NT1 : TFD_GEMV_DEPTH_NT2)
+       : WF == TFD_W_FP8_ROW ? (NT == 1 ? TFD_GEMV_DEPTH_FP8_NT1 : TFD_GEMV_DEPTH_FP8_NT2)
+                             : (NT == 1 ? TFD_GEMV_DEPTH_FP8_NT1 : TFD_GEMV_DEPTH_BLK_NT2);
 }
 
 using namespace tfd;
@@ -59,8 +69,8 @@ struct WTraits<TFD_W_FP8_ROW> {  // 16 codes per thread-row load (16 B)
   static constexpr int E = 16, WORDS = 4, ELEM_BYTES = 1;
 };
 template <>
-struct WTraits<TFD_W_FP8_BLOCK32> {  // 8 codes (8 B): one step = one 32-wide scale block
-  static constexpr int E = 8, WORDS = 2, ELEM_BYTES = 1;
+struct WTraits<TFD_W_FP8_BLOCK32> {  // 2 x 8 codes: 8 from each of the step's two 32-wide blocks
+  static constexpr int E = 16, WORDS = 4, ELEM_BYTES = 1;
 };
 
 struct GemvArgs {
@@ -82,6 +92,8 @@ struct GemvArgs {
   float* top_vals;
   int32_t* top_ids;
   int64_t ldt;  // row stride of top_vals / top_ids
+  float* top1_conf;  // [rows] softmax probability of the top-1, or null
+  float2* part_ms;   // [parts][16] per part (max, sum of exp(l - max)) for the confidence
   int parts;
   int64_t ngroups;
   int ssl;  // steps per k slice
@@ -123,6 +135,13 @@ __device__ __forceinline__ float f16_bits_to_f32(uint16_t b) {
   return __half2float(__ushort_as_half(b));
 }
 
+// Merge of two online-softmax states (max, sum of exp(v - max)).
+__device__ __forceinline__ float2 ms_merge(float2 a, float2 b) {
+  const float m = fmaxf(a.x, b.x);
+  if (m == -INFINITY) return make_float2(-INFINITY, 0.0f);
+  return make_float2(m, a.y * expf(a.x - m) + b.y * expf(b.x - m));
+}
+
 __device__ __forceinline__ float e8m0_scale(uint32_t byte) {
   return byte == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(byte << 23);
 }
@@ -130,7 +149,7 @@ __device__ __forceinline__ float e8m0_scale(uint32_t byte) {
 template <int WF>
 struct WLoad {
   uint32_t r[2][WTraits<WF>::WORDS];  // rows g and g + 8
-  float sc;                           // block scale (FP8_BLOCK32)
+  float sc[2];                        // the step's two block scales (FP8_BLOCK32)
 };
 
 // An fp32 value split into three parts of the MMA operand type (bf16 for bf16 weights, f16 for
@@ -160,7 +179,8 @@ struct Layout {
   __host__ __device__ static size_t x_bytes(int ssl) { return (size_t)PL * 4 * ssl * NT * H * 32 * 16; }
   __host__ __device__ static size_t red_bytes() { return (size_t)2 * kWarps * NT * 32 * 16; }
   __host__ __device__ static size_t best_bytes() {
-    return (size_t)4 * 16 * 8 + 16 * kWarps * 8 + 2 * 16 * 4;  // + per-row x max and x scale
+    // block best keys, join keys, per-row x max and x scale, block (max, sum) pairs, join pairs
+    return (size_t)4 * 16 * 8 + 16 * kWarps * 8 + 2 * 16 * 4 + 4 * 16 * 8 + 16 * kWarps * 8;
   }
   __host__ __device__ static size_t smem_bytes(int ssl) { return x_bytes(ssl) + red_bytes() + best_bytes(); }
 };
@@ -182,6 +202,8 @@ gemv_kernel(const GemvArgs a) {
   uint64_t* sjoin = sbest + 64;
   uint32_t* sxmax = reinterpret_cast<uint32_t*>(sjoin + 16 * kWarps);
   float* sxscale = reinterpret_cast<float*>(sxmax + 16);
+  float2* sms = reinterpret_cast<float2*>(sxscale + 16);   // [4][16]
+  float2* sjms = sms + 64;                                  // [kWarps][16]
   __shared__ int is_last;
   // FP8 weights run f16 MMAs: each activation row is scaled by a power of two 2^-e_r into f16 range
   // (max |x| in [2^14, 2^15)), which keeps every bf16 activation exact down to 2^-32 of the row's
@@ -241,8 +263,10 @@ gemv_kernel(const GemvArgs a) {
       const int k0 = c * 8;
       const int s = k0 / STEPK;
       const int rem = k0 - s * STEPK;
-      const int tt = rem / E;
-      const int hf = (rem - tt * E) >> 3;
+      // A thread's 16-element chunk is contiguous, except in the block-32 form, where it is 8 elements
+      // of each 32-wide scale block of the step (so every MMA stays inside one block).
+      const int tt = WF == TFD_W_FP8_BLOCK32 ? (rem & 31) >> 3 : rem / E;
+      const int hf = WF == TFD_W_FP8_BLOCK32 ? rem >> 5 : (rem - tt * E) >> 3;
       const int ln = (r & 7) * 4 + tt;
       const int nt = r >> 3;
       const bool ok = r < rows && k0 < K;
@@ -305,39 +329,71 @@ gemv_kernel(const GemvArgs a) {
   const float* row_scales = reinterpret_cast<const float*>(a.scales);
   const int64_t kblocks = K >> 5;
 
+  // The thread's first element in a step: its 16 contiguous elements, or (block-32 form) its 8
+  // elements of the step's first 32-wide block, the other 8 being 32 further on.
+  const int toff = WF == TFD_W_FP8_BLOCK32 ? 8 * t : t * E;
+  auto steps_below = [&](int64_t lim) -> int {  // steps s < ssl with (s_begin + s) * STEPK < lim
+    int64_t v = lim > 0 ? (lim + STEPK - 1) / STEPK - s_begin : 0;
+    return (int)(v < 0 ? 0 : (v > ssl ? ssl : v));
+  };
+  const int nvalid = steps_below(K - toff);
+  const int nvalid_b = WF == TFD_W_FP8_BLOCK32 ? steps_below(K - 32 - toff) : nvalid;
+
+  // Load state: group, step, row pointer and row validity; addresses advance by a constant.
   int64_t ld_g = g_begin;
   int ld_s = 0;
+  const unsigned char* lp = nullptr;
+  const uint8_t* sp = nullptr;
+  bool rv0 = false, rv1 = false, rvb = false;
+  auto set_group = [&]() {
+    const int64_t row = ld_g * kGroupRows + mt * 16 + g;
+    const bool in = ld_g < g_end;
+    rv0 = in && row < N;
+    rv1 = in && row + 8 < N;
+    lp = wbase + row * row_bytes + ((int64_t)s_begin * STEPK + toff) * EB;
+    if (WF == TFD_W_FP8_BLOCK32) {
+      const int64_t rblk = (ld_g * kGroupRows + mt * 16) >> 5;
+      rvb = in && rblk * 32 < N;
+      sp = blk_scales + rblk * kblocks + 2 * (int64_t)s_begin;
+    }
+  };
+  set_group();
   auto issue = [&](WLoad<WF>& b) {
 #pragma unroll
     for (int i = 0; i < T::WORDS; ++i) { b.r[0][i] = 0u; b.r[1][i] = 0u; }
-    b.sc = 0.0f;
-    if (ld_g < g_end) {
-      const int64_t row = ld_g * kGroupRows + mt * 16 + g;
-      const int s = s_begin + ld_s;
-      const int64_t kk = (int64_t)s * STEPK + t * E;
-      if (ld_s < ssl && kk < K) {
-        const unsigned char* p0 = wbase + row * row_bytes + kk * EB;
-        if (WF == TFD_W_FP8_BLOCK32) {
-          if (row < N) { uint2 v = ldg_stream8(p0); b.r[0][0] = v.x; b.r[0][1] = v.y; }
-          if (row + 8 < N) {
-            uint2 v = ldg_stream8(p0 + 8 * row_bytes);
-            b.r[1][0] = v.x; b.r[1][1] = v.y;
-          }
-          const int64_t rblk = (ld_g * kGroupRows + mt * 16) >> 5;
-          if (rblk * 32 < N) b.sc = e8m0_scale(__ldg(blk_scales + rblk * kblocks + s));
-        } else {
-          if (row < N) {
-            uint4 v = ldg_stream16(p0);
-            b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
-          }
-          if (row + 8 < N) {
-            uint4 v = ldg_stream16(p0 + 8 * row_bytes);
-            b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
-          }
+    b.sc[0] = 0.0f;
+    b.sc[1] = 0.0f;
+    if (ld_s < nvalid) {
+      if (WF == TFD_W_FP8_BLOCK32) {
+        const bool second = ld_s < nvalid_b;
+        if (rv0) {
+          uint2 v = ldg_stream8(lp);
+          b.r[0][0] = v.x; b.r[0][1] = v.y;
+          if (second) { v = ldg_stream8(lp + 32); b.r[0][2] = v.x; b.r[0][3] = v.y; }
+        }
+        if (rv1) {
+          uint2 v = ldg_stream8(lp + 8 * row_bytes);
+          b.r[1][0] = v.x; b.r[1][1] = v.y;
+          if (second) { v = ldg_stream8(lp + 8 * row_bytes + 32); b.r[1][2] = v.x; b.r[1][3] = v.y; }
+        }
+        if (rvb) {
+          b.sc[0] = e8m0_scale(__ldg(sp));
+          if (second) b.sc[1] = e8m0_scale(__ldg(sp + 1));
+        }
+      } else {
+        if (rv0) {
+          uint4 v = ldg_stream16(lp);
+          b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
+        }
+        if (rv1) {
+          uint4 v = ldg_stream16(lp + 8 * row_bytes);
+          b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
         }
       }
-      if (++ld_s == ssl_loop) { ld_s = 0; ++ld_g; }
     }
+    lp += STEPK * EB;
+    sp += 2;
+    if (++ld_s == ssl_loop) { ld_s = 0; ++ld_g; set_group(); }
   };
 
   // One step: MMA j of the step takes elements [4j, 4j + 4) of each thread's chunk. All activation
@@ -375,16 +431,30 @@ gemv_kernel(const GemvArgs a) {
           if (F16) mma_f16_16816(c[nt], A0, A1, A2, A3, xw[nt][pl][2 * j], xw[nt][pl][2 * j + 1]);
           else mma_bf16_16816(c[nt], A0, A1, A2, A3, xw[nt][pl][2 * j], xw[nt][pl][2 * j + 1]);
         }
+      if (WF == TFD_W_FP8_BLOCK32 && (j & 1)) {
+        // MMAs 0-1 cover the step's first 32-wide block, 2-3 its second: scale each block's sum
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[nt][i] = fmaf(b.sc[j >> 1], c[nt][i], acc[nt][i]);
+            c[nt][i] = 0.0f;
+          }
+      }
     }
+    if (WF != TFD_W_FP8_BLOCK32) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        acc[nt][i] = (WF == TFD_W_FP8_BLOCK32) ? fmaf(b.sc, c[nt][i], acc[nt][i]) : c[nt][i];
+        for (int i = 0; i < 4; ++i) acc[nt][i] = c[nt][i];
+    }
   };
 
   // Epilogue of one output value: scale, store, rank.
   uint64_t best[2] = {0ull, 0ull};
+  // online softmax state (max, sum of exp(v - max)) of this thread's outputs, for the confidence
+  float2 ms[2] = {make_float2(-INFINITY, 0.0f), make_float2(-INFINITY, 0.0f)};
+  const bool want_conf = a.topk == 1 && a.top1_conf != nullptr;
   auto epi = [&](int64_t row, int act, float v, int slot) {
     if (row >= N || act >= rows) return;
     if (F16) v *= sxscale[act];
@@ -401,6 +471,14 @@ gemv_kernel(const GemvArgs a) {
     if (a.topk == 1) {
       const int32_t id = a.id_map ? __ldg(a.id_map + row) : (int32_t)row;
       best[slot] = umax64(best[slot], make_key(v, id));
+      if (want_conf && v > -INFINITY) {  // NaN and -inf add nothing
+        if (v > ms[slot].x) {
+          ms[slot].y = ms[slot].y * expf(ms[slot].x - v) + 1.0f;
+          ms[slot].x = v;
+        } else {
+          ms[slot].y += expf(v - ms[slot].x);
+        }
+      }
     } else if (a.logits != nullptr && a.logits != a.y) {
       a.logits[(int64_t)act * a.ld_logits + row] = v;
     }
@@ -462,12 +540,24 @@ gemv_kernel(const GemvArgs a) {
       key = umax64(key, shfl_xor_u64(key, 8));
       key = umax64(key, shfl_xor_u64(key, 16));
       if (g == 0) sbest[mr * 16 + nr * 8 + 2 * t + c] = key;
+      if (want_conf) {
+        float2 q = ms[c];
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1)
+          q = ms_merge(q, make_float2(__shfl_xor_sync(0xffffffffu, q.x, o),
+                                      __shfl_xor_sync(0xffffffffu, q.y, o)));
+        if (g == 0) sms[mr * 16 + nr * 8 + 2 * t + c] = q;
+      }
     }
   }
   __syncthreads();
   if (tid < kMaxRowsPad) {
     uint64_t m = umax64(umax64(sbest[tid], sbest[16 + tid]), umax64(sbest[32 + tid], sbest[48 + tid]));
     a.part_keys[(int64_t)blockIdx.x * kMaxRowsPad + tid] = m;
+    if (want_conf) {
+      const float2 q = ms_merge(ms_merge(sms[tid], sms[16 + tid]), ms_merge(sms[32 + tid], sms[48 + tid]));
+      a.part_ms[(int64_t)blockIdx.x * kMaxRowsPad + tid] = q;
+    }
   }
   __threadfence();
   __syncthreads();
@@ -490,12 +580,30 @@ gemv_kernel(const GemvArgs a) {
     for (int o = 16; o > 0; o >>= 1) key = umax64(key, shfl_xor_u64(key, o));
     if (lane == 0) sjoin[warp * kMaxRowsPad + r] = key;
   }
+  if (want_conf) {
+    // parts are merged in a fixed order: p = tid, tid + 512, ..., then lanes, then warps
+    for (int r = 0; r < rows; ++r) {
+      float2 q = make_float2(-INFINITY, 0.0f);
+      for (int p = tid; p < a.parts; p += kThreads)
+        q = ms_merge(q, __ldcg(a.part_ms + (int64_t)p * kMaxRowsPad + r));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+        q = ms_merge(q, make_float2(__shfl_xor_sync(0xffffffffu, q.x, o),
+                                    __shfl_xor_sync(0xffffffffu, q.y, o)));
+      if (lane == 0) sjms[warp * kMaxRowsPad + r] = q;
+    }
+  }
   __syncthreads();
   if (tid < rows) {
     uint64_t key = 0ull;
     for (int w = 0; w < kWarps; ++w) key = umax64(key, sjoin[w * kMaxRowsPad + tid]);
     a.top_vals[tid * a.ldt] = key_value(key);
     a.top_ids[tid * a.ldt] = key_id(key);
+    if (want_conf) {
+      float2 q = make_float2(-INFINITY, 0.0f);
+      for (int w = 0; w < kWarps; ++w) q = ms_merge(q, sjms[w * kMaxRowsPad + tid]);
+      a.top1_conf[tid] = q.y > 0.0f ? 1.0f / q.y : __uint_as_float(0x7FC00000u);
+    }
   }
   if (tid == 0) *a.counter = 0u;  // leave the workspace zeroed
 }
@@ -568,6 +676,7 @@ size_t gemv_smem_any(int wfmt, int xfmt, int rows, int64_t k) {
 struct GemvWs {
   uint32_t* counter;
   uint64_t* part_keys;
+  float2* part_ms;
   float* logits;
   void* topk_ws;
   size_t topk_bytes;
@@ -576,12 +685,14 @@ struct GemvWs {
 // Workspace: [counter | part keys for top-1 | fp32 logits for top-k > 1 | top-k workspace].
 size_t gemv_ws_layout(int rows, int64_t n, int topk, bool logits_in_y, char* base, GemvWs* out) {
   size_t off = 256;
-  size_t keys = topk == 1 ? tfd_host::round_up((size_t)kMaxParts * kMaxRowsPad * 8, 256) : 0;
+  // top-1: per part a key and an online-softmax pair per row
+  size_t keys = topk == 1 ? tfd_host::round_up((size_t)kMaxParts * kMaxRowsPad * 8, 256) * 2 : 0;
   size_t lg = (topk > 1 && !logits_in_y) ? tfd_host::round_up((size_t)rows * n * 4, 256) : 0;
   size_t tk = topk > 1 ? tfd_internal::topk_workspace(rows, n, topk) : 0;
   if (out) {
     out->counter = reinterpret_cast<uint32_t*>(base);
     out->part_keys = keys ? reinterpret_cast<uint64_t*>(base + off) : nullptr;
+    out->part_ms = keys ? reinterpret_cast<float2*>(base + off + keys / 2) : nullptr;
     out->logits = lg ? reinterpret_cast<float*>(base + off + keys) : nullptr;
     out->topk_ws = tk ? base + off + keys + lg : nullptr;
     out->topk_bytes = tk;
@@ -622,8 +733,8 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
                                     int64_t k, const void* x, int xfmt, int rows, int64_t ldx,
                                     int out_mode, void* y, int64_t ldy, int topk, int parts,
                                     const int32_t* id_map, float* top_vals, int32_t* top_ids,
-                                    int64_t ldt, void* ws, size_t ws_bytes, int32_t* dev_status,
-                                    void* stream) {
+                                    int64_t ldt, float* top1_conf, void* ws, size_t ws_bytes,
+                                    int32_t* dev_status, void* stream) {
   using tfd_host::aligned;
   (void)dev_status;  // no device-data errors are possible in this call
   if (!w || !x) return TFD_ERR_INVALID;
@@ -643,6 +754,7 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
     return TFD_ERR_INVALID;
   if (ldt == 0) ldt = topk;
   if (topk > 0 && ldt < topk) return TFD_ERR_INVALID;
+  if (top1_conf && (topk != 1 || !aligned(top1_conf, 4))) return TFD_ERR_INVALID;
   if (parts < 0 || parts > kMaxParts) return TFD_ERR_INVALID;
   if (id_map && !aligned(id_map, 4)) return TFD_ERR_INVALID;
   const size_t yb = out_mode == TFD_OUT_F32 ? 4 : 2;
@@ -670,6 +782,8 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   a.top_vals = top_vals;
   a.top_ids = top_ids;
   a.ldt = ldt;
+  a.top1_conf = top1_conf;
+  a.part_ms = wl.part_ms;
   a.ngroups = (n + kGroupRows - 1) / kGroupRows;
   cudaStream_t s = tfd_host::as_stream(stream);
   tfd_status st;

@@ -46,8 +46,8 @@ extern "C" tfd_status tfd_head_gemv_noalloc(const void* w, int wfmt, const void*
                                             int rows, int64_t ldx, int out_mode, void* y,
                                             int64_t ldy, int topk, int parts,
                                             const int32_t* id_map, float* top_vals,
-                                            int32_t* top_ids, int64_t ldt, int32_t* dev_status,
-                                            void* stream) {
+                                            int32_t* top_ids, int64_t ldt, float* top1_conf,
+                                            int32_t* dev_status, void* stream) {
   const size_t need = tfd_head_gemv_workspace(rows, n, topk, parts);
   if (need > (size_t)TFD_NOALLOC_SCRATCH_BYTES) return TFD_ERR_WORKSPACE;
   void* ws = nullptr;
@@ -59,5 +59,5 @@ extern "C" tfd_status tfd_head_gemv_noalloc(const void* w, int wfmt, const void*
       return TFD_ERR_CUDA;
   }
   return tfd_head_gemv(w, wfmt, w_scales, n, k, x, xfmt, rows, ldx, out_mode, y, ldy, topk, parts,
-                       id_map, top_vals, top_ids, ldt, ws, need, dev_status, stream);
+                       id_map, top_vals, top_ids, ldt, top1_conf, ws, need, dev_status, stream);
 }

@@ -10,6 +10,7 @@ constexpr int kSelectMaxK = 512;
 
 struct SelectSmem {
   uint64_t out[kSelectMaxK];     // selected keys (then sorted in place)
+  uint32_t whist[kSelectThreads / 64][256];  // one histogram per pair of warps
   uint32_t hist[256];
   int found_digit;
   int found_above;
@@ -21,14 +22,14 @@ struct SelectSmem {
 // Selects the min(k, cnt) largest of cnt keys (k <= kSelectMaxK) produced by key_at(i), i in
 // [0, cnt), into sm.out[0..min(k, cnt)), sorted descending. Keys are unique except for exact duplicates,
 // which are interchangeable. The radix descent histograms 8 bits of the key per pass among the
-// keys that share the prefix found so far, stopping as soon as the boundary bin is taken whole.
+// keys that share the prefix found so far (shared-memory histograms per pair of warps, then summed),
+// stopping as soon as the boundary bin is taken whole.
 // Must be called by all kSelectThreads threads of the block.
 template <class KeyAt>
-__device__ void block_select_topk(int cnt, int k, KeyAt key_at, SelectSmem& sm) {
+__device__ void block_select_topk(int cnt, int k, KeyAt key_at, SelectSmem& sm, bool sort = true) {
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int cnt_round = (cnt + 31) & ~31;
 
   __syncthreads();  // the previous use of sm is finished
   if (tid == 0) { sm.out_count = 0; sm.eq_count = 0; }
@@ -41,15 +42,20 @@ __device__ void block_select_topk(int cnt, int k, KeyAt key_at, SelectSmem& sm) 
     whole_bin = false;
     for (int pass = 0; pass < 8; ++pass) {
       shift -= 8;
-      for (int b = tid; b < 256; b += kSelectThreads) sm.hist[b] = 0;
+      for (int b = tid; b < (kSelectThreads / 64) * 256; b += kSelectThreads)
+        (&sm.whist[0][0])[b] = 0;
       __syncthreads();
-      for (int i = tid; i < cnt_round; i += kSelectThreads) {
-        bool valid = i < cnt;
-        uint64_t key = valid ? key_at(i) : 0ull;
-        bool match = valid && (shift == 56 || (key >> (shift + 8)) == prefix);
-        int bin = match ? (int)((key >> shift) & 255u) : 256;
-        unsigned peers = __match_any_sync(0xffffffffu, bin);
-        if (bin < 256 && (__ffs(peers) - 1) == lane) atomicAdd(&sm.hist[bin], __popc(peers));
+      for (int i = tid; i < cnt; i += kSelectThreads) {
+        const uint64_t key = key_at(i);
+        if (shift == 56 || (key >> (shift + 8)) == prefix)
+          atomicAdd(&sm.whist[warp >> 1][(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      for (int b = tid; b < 256; b += kSelectThreads) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int w = 0; w < kSelectThreads / 64; ++w) c += sm.whist[w][b];
+        sm.hist[b] = c;
       }
       __syncthreads();
       if (warp == 0) {
@@ -108,6 +114,7 @@ __device__ void block_select_topk(int cnt, int k, KeyAt key_at, SelectSmem& sm) 
     }
   }
   __syncthreads();
+  if (!sort) return;
   // Bitonic sort of the min(k, cnt) selected keys, descending (padded with zero keys).
   const int kk = cnt < k ? cnt : k;
   int kpad = 1;
@@ -127,6 +134,120 @@ __device__ void block_select_topk(int cnt, int k, KeyAt key_at, SelectSmem& sm) 
       __syncthreads();
     }
   }
+}
+
+// One warp sorts a[0..n) descending in shared memory (n a power of two, <= 1024).
+__device__ inline void warp_sort_desc(uint64_t* a, int n) {
+  const int lane = threadIdx.x & 31;
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      for (int t = lane; t < (n >> 1); t += 32) {
+        const int i = 2 * t - (t & (j - 1));
+        const uint64_t x = a[i], y = a[i + j];
+        if (((i & size) == 0) ? (x < y) : (x > y)) { a[i] = y; a[i + j] = x; }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+constexpr int kDigitBits = 12;
+constexpr int kBins = 1 << kDigitBits;
+constexpr int kCandCap = 2048;     // keys at or above the boundary bin that are ranked directly
+constexpr int kRankDirect = 1024;  // at most this many keys are ranked without a histogram
+
+struct FastSelectSmem {
+  uint32_t hist[kBins];
+  uint64_t cand[kCandCap];
+  int warp_sum[kSelectThreads / 32];
+  int bstar, n_cand;
+};
+
+// out[rank] = key for the keys of c[0..n) whose rank (number of keys that beat it; equal keys are
+// ordered by position) is below k: the top min(k, n) in descending order. One broadcast read of
+// each candidate per thread; no sorting network.
+__device__ inline void rank_count_select(const uint64_t* c, int n, int k, uint64_t* out) {
+  const int tid = threadIdx.x;
+  for (int i0 = tid; i0 < n; i0 += 2 * kSelectThreads) {
+    const int i1 = i0 + kSelectThreads;
+    const uint64_t a = c[i0];
+    const uint64_t b = i1 < n ? c[i1] : 0ull;
+    int ra = 0, rb = 0;
+    for (int j = 0; j < n; ++j) {
+      const uint64_t x = c[j];
+      ra += (x > a) | ((x == a) & (j < i0));
+      rb += (x > b) | ((x == b) & (j < i1));
+    }
+    if (ra < k) out[ra] = a;
+    if (i1 < n && rb < k) out[rb] = b;
+  }
+  __syncthreads();
+}
+
+// Top min(k, cnt) of keys[0..cnt) (shared memory), descending, written to out[0..min(k, cnt)).
+// Small inputs are ranked directly. Otherwise one histogram of the top 12 key bits finds the bin
+// holding the k-th key, every key in that bin or above is gathered (warp-aggregated appends) and
+// ranked. Degenerate inputs (more than kCandCap keys at or above that bin) use the radix descent.
+// Called by all kSelectThreads threads of the block.
+__device__ inline void block_topk_fast(int cnt, int k, const uint64_t* keys, uint64_t* out,
+                                       FastSelectSmem& fs, SelectSmem& sel) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __syncthreads();
+  if (cnt <= kRankDirect || cnt <= k) {
+    rank_count_select(keys, cnt, k, out);
+    return;
+  }
+  for (int b = tid; b < kBins; b += kSelectThreads) fs.hist[b] = 0u;
+  if (tid == 0) fs.n_cand = 0;
+  __syncthreads();
+  for (int i = tid; i < cnt; i += kSelectThreads)
+    atomicAdd(&fs.hist[keys[i] >> (64 - kDigitBits)], 1u);
+  __syncthreads();
+  constexpr int per = kBins / kSelectThreads;  // bins [per * tid, per * tid + per) per thread
+  uint32_t c[per];
+  int mine = 0;
+#pragma unroll
+  for (int j = 0; j < per; ++j) { c[j] = fs.hist[per * tid + j]; mine += (int)c[j]; }
+  int incl = mine;  // suffix sum over the warp's lanes (higher lanes own higher bins)
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += v;
+  }
+  if (lane == 0) fs.warp_sum[warp] = incl;
+  __syncthreads();
+  int above = incl - mine;
+  for (int w = warp + 1; w < kSelectThreads / 32; ++w) above += fs.warp_sum[w];
+  if (above < k && above + mine >= k) {
+#pragma unroll
+    for (int j = per - 1; j >= 0; --j) {
+      if (above + (int)c[j] >= k) { fs.bstar = per * tid + j; break; }
+      above += (int)c[j];
+    }
+  }
+  __syncthreads();
+  const uint64_t bstar = (uint64_t)fs.bstar;
+  const int rounds = (cnt + kSelectThreads - 1) / kSelectThreads;
+  for (int r = 0; r < rounds; ++r) {  // whole warps iterate together for the ballot
+    const int i = r * kSelectThreads + tid;
+    const uint64_t key = i < cnt ? keys[i] : 0ull;
+    const bool take = i < cnt && (key >> (64 - kDigitBits)) >= bstar;
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    int base = 0;
+    if (lane == 0 && m) base = atomicAdd(&fs.n_cand, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int at = base + __popc(m & ((1u << lane) - 1u));
+    if (take && at < kCandCap) fs.cand[at] = key;
+  }
+  __syncthreads();
+  const int ncand = fs.n_cand;
+  if (ncand > kCandCap) {
+    block_select_topk(cnt, k, [&](int i) { return keys[i]; }, sel, true);
+    for (int i = tid; i < k; i += kSelectThreads) out[i] = sel.out[i];
+    __syncthreads();
+    return;
+  }
+  rank_count_select(fs.cand, ncand, k, out);
 }
 
 }  // namespace tfd

@@ -1,5 +1,9 @@
-// topk.cu - split top-k over given fp32 logits: each (row, part) block keeps the exact top-k of a
-// contiguous range, and the last block of a row to finish joins the parts' lists.
+// topk.cu - split top-k over given fp32 logits: each (row, part) block stages a contiguous range
+// of 8192 keys in shared memory and selects its top k there; the last block of a row to finish
+// stages the union of the parts' lists in shared memory and selects the row's top k from it. A
+// selection is one histogram pass to a boundary bin, a gather of the keys at or above it, and a
+// rank count (each key's rank is the number of keys that beat it: the rank-count top-k of the
+// subset page (#1011), "tf_super_topk_few").
 //
 // Follows the TFE draft head page (#42): commit "... ocabulary head" (top cand_k of fp32 logits,
 // 1..512, a tie at the k-th value going to the lower token id; the top-1 through an id map) and
@@ -10,152 +14,139 @@ namespace {
 
 using namespace tfd;
 
-constexpr int kStage = 4096;  // keys a block holds in shared memory (part length cap)
+constexpr int kCap = 16384;  // keys a block holds in shared memory (a part, or the join's union)
+constexpr int kPartLen = 8192;  // keys per part
 
 struct TopkPlan {
   int parts;
   int64_t chunk;
+  int64_t cap;  // shared-memory keys per block: max(chunk, parts * k), or chunk when the union
+                // does not fit (then the join reads the lists from global memory)
 };
 
-// Parts per row: at least n / 4096 (a part fits in shared memory), and about 320 blocks in all
-// when the row is long enough for parts of max(4k, 1024). Independent of the device.
+// Parts per row: n / 8192 (at least 1), fewer when the join's union of part lists (parts * k
+// keys) would not fit in shared memory. Independent of the device.
 TopkPlan topk_plan(int rows, int64_t n, int k) {
-  int64_t want = (320 + rows - 1) / rows;
-  int64_t min_len = 4LL * k > 1024 ? 4LL * k : 1024;
-  int64_t by_len = n / min_len;
-  if (want > by_len) want = by_len;
-  int64_t need = (n + kStage - 1) / kStage;
-  int64_t p = want > need ? want : need;
+  (void)rows;
+  int64_t p = (n + kPartLen - 1) / kPartLen;
+  int64_t by_join = kCap / k;
+  if (p > by_join) p = by_join;
+  int64_t need = (n + kCap - 1) / kCap;
+  if (p < need) p = need;
   if (p < 1) p = 1;
   int64_t chunk = (n + p - 1) / p;
   p = (n + chunk - 1) / chunk;
-  return TopkPlan{(int)p, chunk};
+  int64_t uni = p * k;
+  int64_t cap = uni <= kCap ? (uni > chunk ? uni : chunk) : chunk;
+  return TopkPlan{(int)p, chunk, cap};
 }
 
 struct TopkWs {
   uint32_t* counters;  // [rows]
   int* counts;         // [rows][parts]  keys each part kept
-  uint64_t* kth;       // [rows][parts]  the part's k-th key (0 when it kept fewer than k)
   uint64_t* keys;      // [rows][parts][k], each part's list sorted descending
 };
 
 size_t topk_ws_layout(int rows, int parts, int k, char* base, TopkWs* out) {
   size_t c_bytes = tfd_host::round_up((size_t)rows * 4, 256);
   size_t n_bytes = tfd_host::round_up((size_t)rows * parts * 4, 256);
-  size_t t_bytes = tfd_host::round_up((size_t)rows * parts * 8, 256);
   size_t k_bytes = tfd_host::round_up((size_t)rows * parts * k * 8, 256);
   if (out) {
     out->counters = reinterpret_cast<uint32_t*>(base);
     out->counts = reinterpret_cast<int*>(base + c_bytes);
-    out->kth = reinterpret_cast<uint64_t*>(base + c_bytes + n_bytes);
-    out->keys = reinterpret_cast<uint64_t*>(base + c_bytes + n_bytes + t_bytes);
+    out->keys = reinterpret_cast<uint64_t*>(base + c_bytes + n_bytes);
   }
-  return c_bytes + n_bytes + t_bytes + k_bytes;
+  return c_bytes + n_bytes + k_bytes;
 }
 
-struct TopkSmem {
-  SelectSmem sel;
-  uint64_t keys[kStage];
-  uint64_t red[kSelectThreads / 32];
-  int scan[kSelectThreads / 32];
-  int total;
-  int is_last;
-};
+size_t topk_smem_fixed() { return sizeof(SelectSmem) + sizeof(FastSelectSmem) + 16; }
+size_t topk_smem_bytes(const TopkPlan& pl) { return topk_smem_fixed() + (size_t)pl.cap * 8; }
+
+__device__ __forceinline__ size_t topk_smem_fixed_dev() {
+  return sizeof(SelectSmem) + sizeof(FastSelectSmem) + 16;
+}
 
 __global__ void __launch_bounds__(kSelectThreads)
 topk_kernel(const float* __restrict__ logits, int64_t n, int64_t ld, int k,
             const int32_t* __restrict__ id_map, float* __restrict__ vals,
-            int32_t* __restrict__ ids, int64_t ld_out, TopkWs ws, int parts, int64_t chunk) {
-  __shared__ TopkSmem sm;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+            int32_t* __restrict__ ids, int64_t ld_out, TopkWs ws, int parts, int64_t chunk,
+            int64_t cap) {
+  extern __shared__ __align__(16) unsigned char tk_smem[];
+  SelectSmem& sel = *reinterpret_cast<SelectSmem*>(tk_smem);
+  FastSelectSmem& fs = *reinterpret_cast<FastSelectSmem*>(tk_smem + sizeof(SelectSmem));
+  int* is_last = reinterpret_cast<int*>(tk_smem + sizeof(SelectSmem) + sizeof(FastSelectSmem));
+  uint64_t* keys = reinterpret_cast<uint64_t*>(tk_smem + topk_smem_fixed_dev());
+  const int tid = threadIdx.x;
   const int p = blockIdx.x;
   const int r = blockIdx.y;
   const int64_t lo = (int64_t)p * chunk;
   const int64_t hi = lo + chunk < n ? lo + chunk : n;
-  const int cnt = hi > lo ? (int)(hi - lo) : 0;  // <= kStage by the plan
+  const int cnt = hi > lo ? (int)(hi - lo) : 0;  // <= cap by the plan
   const float* row = logits + (int64_t)r * ld;
 
-  // ---- part: stage its keys in shared memory, select, publish the sorted list and its k-th ----
-  for (int i = tid; i < cnt; i += kSelectThreads) {
-    const int64_t j = lo + i;
-    sm.keys[i] = make_key(row[j], id_map ? id_map[j] : (int32_t)j);
+  // ---- part: stage its keys in shared memory, select its top kk, publish the sorted list ----
+  // 8 independent loads in flight per thread before any store
+  for (int i0 = tid; i0 < cnt; i0 += 8 * kSelectThreads) {
+    float v[8];
+    int32_t id[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kSelectThreads;
+      const int64_t j = lo + (i < cnt ? i : 0);
+      v[u] = row[j];
+      id[u] = id_map ? id_map[j] : (int32_t)j;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kSelectThreads;
+      if (i < cnt) keys[i] = make_key(v[u], id[u]);
+    }
   }
-  block_select_topk(cnt, k, [&](int i) { return sm.keys[i]; }, sm.sel);
   const int kk = cnt < k ? cnt : k;
+  block_topk_fast(cnt, k, keys, sel.out, fs, sel);
   uint64_t* dst = ws.keys + ((int64_t)r * parts + p) * k;
-  for (int i = tid; i < kk; i += kSelectThreads) dst[i] = sm.sel.out[i];
-  if (tid == 0) {
-    ws.counts[r * parts + p] = kk;
-    ws.kth[r * parts + p] = kk == k ? sm.sel.out[k - 1] : 0ull;
-  }
+  for (int i = tid; i < kk; i += kSelectThreads) dst[i] = sel.out[i];
+  if (tid == 0) ws.counts[r * parts + p] = kk;
   __threadfence();
   __syncthreads();
-  if (tid == 0) sm.is_last = (atomicAdd(&ws.counters[r], 1u) == (uint32_t)(parts - 1));
+  if (tid == 0) *is_last = (atomicAdd(&ws.counters[r], 1u) == (uint32_t)(parts - 1));
   __syncthreads();
-  if (!sm.is_last) return;
+  if (!*is_last) return;
   __threadfence();
 
-  // ---- join: every key of the row's top-k is >= L = max over parts of the part's k-th key (the
-  // part holding L has k keys >= L), so only each sorted list's prefix >= L takes part ----
+  // ---- join: the row's top k is the top k of the union of the parts' lists ----
   const uint64_t* rowkeys = ws.keys + (int64_t)r * parts * k;
   const int* rowcounts = ws.counts + r * parts;
-  uint64_t L = 0ull;
-  for (int q = tid; q < parts; q += kSelectThreads) L = umax64(L, __ldcg(ws.kth + r * parts + q));
+  const int uni = parts * k;
+  __syncthreads();
+  if ((int64_t)uni <= cap) {
+    for (int i0 = tid; i0 < uni; i0 += 8 * kSelectThreads) {
+      uint64_t kv[8];
+      int cq[8];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L = umax64(L, shfl_xor_u64(L, o));
-  if (lane == 0) sm.red[warp] = L;
-  __syncthreads();
-  L = 0ull;
-  for (int w = 0; w < kSelectThreads / 32; ++w) L = umax64(L, sm.red[w]);
-  // survivors of each part (binary search of its descending list); thread tid owns parts
-  // tid, tid + 512, ... and their survivors are placed after an exclusive scan.
-  int mine = 0;
-  for (int q = tid; q < parts; q += kSelectThreads) {
-    const uint64_t* lst = rowkeys + (int64_t)q * k;
-    int a = 0, b = __ldcg(rowcounts + q);  // first index with key < L lies in [a, b]
-    while (a < b) {
-      int m = (a + b) >> 1;
-      if (__ldcg(lst + m) >= L) a = m + 1; else b = m;
-    }
-    mine += a;
-  }
-  int incl = mine;
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kSelectThreads;
+        const int ii = i < uni ? i : 0;
+        kv[u] = __ldcg(rowkeys + ii);
+        cq[u] = __ldcg(rowcounts + ii / k);
+      }
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) sm.scan[warp] = incl;
-  __syncthreads();
-  int before = 0;
-  for (int w = 0; w < warp; ++w) before += sm.scan[w];
-  if (tid == kSelectThreads - 1) sm.total = before + incl;
-  __syncthreads();
-  const int total = sm.total;
-  if (total <= kStage) {
-    int at = before + incl - mine;
-    for (int q = tid; q < parts; q += kSelectThreads) {
-      const uint64_t* lst = rowkeys + (int64_t)q * k;
-      const int c = __ldcg(rowcounts + q);
-      for (int i = 0; i < c; ++i) {
-        const uint64_t key = __ldcg(lst + i);
-        if (key < L) break;
-        sm.keys[at++] = key;
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kSelectThreads;
+        if (i < uni) keys[i] = (i % k) < cq[u] ? kv[u] : 0ull;
       }
     }
-    block_select_topk(total, k, [&](int i) { return sm.keys[i]; }, sm.sel);
+    block_topk_fast(uni, k, keys, sel.out, fs, sel);
   } else {
-    // many near-equal keys at L: select from every list in global memory
     auto join_key = [&](int i) -> uint64_t {
-      int q = i / k;
-      int j = i - q * k;
-      return j < __ldcg(rowcounts + q) ? __ldcg(rowkeys + i) : 0ull;
+      const int q = i / k;
+      return (i - q * k) < __ldcg(rowcounts + q) ? __ldcg(rowkeys + i) : 0ull;
     };
-    block_select_topk(parts * k, k, join_key, sm.sel);
+    block_select_topk(uni, k, join_key, sel);
   }
   for (int i = tid; i < k; i += kSelectThreads) {
-    vals[(int64_t)r * ld_out + i] = key_value(sm.sel.out[i]);
-    ids[(int64_t)r * ld_out + i] = key_id(sm.sel.out[i]);
+    vals[(int64_t)r * ld_out + i] = key_value(sel.out[i]);
+    ids[(int64_t)r * ld_out + i] = key_id(sel.out[i]);
   }
   if (tid == 0) ws.counters[r] = 0u;  // leave the workspace counters at zero
 }
@@ -177,9 +168,13 @@ tfd_status topk_launch(const float* logits, int rows, int64_t n, int64_t ld, int
   TopkWs w;
   size_t need = topk_ws_layout(rows, pl.parts, k, reinterpret_cast<char*>(ws), &w);
   if (ws == nullptr || ws_bytes < need) return TFD_ERR_WORKSPACE;
+  const size_t smem = topk_smem_bytes(pl);
+  if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(topk_smem_fixed() + (size_t)kCap * 8)) != cudaSuccess)
+    return TFD_ERR_CUDA;
   dim3 grid(pl.parts, rows);
-  topk_kernel<<<grid, kSelectThreads, 0, stream>>>(logits, n, ld, k, id_map, vals, ids, ld_out,
-                                                   w, pl.parts, pl.chunk);
+  topk_kernel<<<grid, kSelectThreads, smem, stream>>>(logits, n, ld, k, id_map, vals, ids, ld_out,
+                                                      w, pl.parts, pl.chunk, pl.cap);
   return tfd_host::launch_status();
 }
 

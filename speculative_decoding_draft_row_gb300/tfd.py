@@ -28,9 +28,9 @@ SIGNATURES = {
     "tfd_head_gemv_workspace": (_sz, [_i32, _i64, _i32, _i32]),
     "tfd_head_gemv_max_k": (_i64, [_i32, _i32]),
     "tfd_head_gemv": (_i32, [_vp, _i32, _vp, _i64, _i64, _vp, _i32, _i32, _i64, _i32, _vp, _i64,
-                             _i32, _i32, _vp, _vp, _vp, _i64, _vp, _sz, _vp, _vp]),
+                             _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _sz, _vp, _vp]),
     "tfd_head_gemv_noalloc": (_i32, [_vp, _i32, _vp, _i64, _i64, _vp, _i32, _i32, _i64, _i32,
-                                     _vp, _i64, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp]),
+                                     _vp, _i64, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _vp]),
     "tfd_topk_workspace": (_sz, [_i32, _i64, _i32]),
     "tfd_topk": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "tfd_rescore_workspace": (_sz, [_i32, _i32]),
@@ -128,8 +128,10 @@ def tfd_head_gemv_max_k(rows, xfmt=X_BF16):
 
 
 def tfd_head_gemv(w, wfmt, w_scales, x, out_mode=OUT_F32, y=None, topk=0, parts=0, id_map=None,
-                  top_vals=None, top_ids=None, ws=None, dev_status=None, n=None, stream=None):
-    """Few-row head GEMV with optional output and fused top-k. Returns (y, top_vals, top_ids)."""
+                  top_vals=None, top_ids=None, ws=None, dev_status=None, n=None, top1_conf=None,
+                  stream=None):
+    """Few-row head GEMV with optional output and fused top-k (top-1 optionally with its softmax
+    probability in ``top1_conf`` [rows]). Returns (y, top_vals, top_ids)."""
     _dev(w, x, y, id_map, ws)
     n = w.shape[0] if n is None else n
     k = w.shape[1]
@@ -150,17 +152,18 @@ def tfd_head_gemv(w, wfmt, w_scales, x, out_mode=OUT_F32, y=None, topk=0, parts=
         raise ValueError("top_vals and top_ids must share their row stride")
     st = library().tfd_head_gemv(_p(w), wfmt, _p(w_scales), n, k, _p(x), xfmt, rows, x.stride(0),
                                  out_mode, _p(y), ldy, topk, parts, _p(id_map), _p(top_vals),
-                                 _p(top_ids), ldt, _p(ws), ws_bytes, _p(dev_status),
-                                 _stream(stream))
+                                 _p(top_ids), ldt, _p(top1_conf), _p(ws), ws_bytes,
+                                 _p(dev_status), _stream(stream))
     _check("tfd_head_gemv", st)
     return y, top_vals, top_ids
 
 
-NOALLOC_SCRATCH_BYTES = 262144
+NOALLOC_SCRATCH_BYTES = 524288
 
 
 def tfd_head_gemv_noalloc(w, wfmt, w_scales, x, out_mode=OUT_F32, y=None, topk=0, parts=0,
-                          id_map=None, top_vals=None, top_ids=None, dev_status=None, stream=None):
+                          id_map=None, top_vals=None, top_ids=None, dev_status=None,
+                          top1_conf=None, stream=None):
     """tfd_head_gemv on the library's fixed scratch (no workspace argument): for callers that
     cannot allocate device memory. Outputs must be passed in by such callers; the defaults here
     allocate them only for convenience. Returns (y, top_vals, top_ids)."""
@@ -179,7 +182,7 @@ def tfd_head_gemv_noalloc(w, wfmt, w_scales, x, out_mode=OUT_F32, y=None, topk=0
                                          x.stride(0), out_mode, _p(y),
                                          y.stride(0) if y is not None else 0, topk, parts,
                                          _p(id_map), _p(top_vals), _p(top_ids), ldt,
-                                         _p(dev_status), _stream(stream))
+                                         _p(top1_conf), _p(dev_status), _stream(stream))
     _check("tfd_head_gemv_noalloc", st)
     return y, top_vals, top_ids
 

@@ -56,12 +56,13 @@ FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced by refu
 def gemv(**kw):
     a = dict(w=FAKE, wfmt=0, ws_=None, n=4096, k=256, x=FAKE, xfmt=0, rows=1, ldx=256, out=1,
              y=FAKE * 2, ldy=4096, topk=0, parts=0, id_map=None, tv=None, ti=None, ldt=0,
-             ws=None, wsb=0, st=None, stream=None)
+             conf=None, ws=None, wsb=0, st=None, stream=None)
     a.update(kw)
     return tfd.library().tfd_head_gemv(a["w"], a["wfmt"], a["ws_"], a["n"], a["k"], a["x"],
                                        a["xfmt"], a["rows"], a["ldx"], a["out"], a["y"], a["ldy"],
                                        a["topk"], a["parts"], a["id_map"], a["tv"], a["ti"],
-                                       a["ldt"], a["ws"], a["wsb"], a["st"], a["stream"])
+                                       a["ldt"], a["conf"], a["ws"], a["wsb"], a["st"],
+                                       a["stream"])
 
 
 @pytest.mark.parametrize("bad,code", [
@@ -71,6 +72,7 @@ def gemv(**kw):
     (dict(y=None), 1), (dict(ldy=10), 1), (dict(topk=513), 1), (dict(topk=1), 1),
     (dict(topk=1, tv=FAKE, ti=FAKE), 3), (dict(parts=-1), 1), (dict(parts=5000), 1),
     (dict(topk=8, tv=FAKE, ti=FAKE, ldt=4), 1),
+    (dict(topk=8, tv=FAKE, ti=FAKE, conf=FAKE * 4), 1),   # confidence only with top-1
     (dict(y=FAKE), 1),  # y overlaps x
     (dict(rows=16, k=65536, ldx=65536, y=FAKE * 64), 2),  # activation tile past shared memory
 ])

@@ -8,6 +8,7 @@ from helpers import (assert_bf16_close, assert_fp32_close, assert_sorted_keys, a
                      need_gpu, np32, same_bits)
 from oracle import gemv as og
 from oracle.quant import quant_fp8_block32, quant_fp8_row
+from oracle.topk import top1_confidence
 from oracle.topk import topk as oracle_topk
 from speculative_decoding_draft_row_gb300 import tfd
 from synth import inputs
@@ -112,6 +113,27 @@ def test_fused_topk_matches_own_logits_and_oracle(wfmt):
         assert np.array_equal(ti2.cpu().numpy(), oi) and same_bits(np32(tv2), ov)
         assert_sorted_keys(np32(tv), ti.cpu().numpy())
         assert_topk_valid(np32(tv), ti.cpu().numpy(), acc, S, k, what=f"top-{k}")
+
+
+@pytest.mark.parametrize("wfmt,rows", [(tfd.W_BF16, 1), (tfd.W_BF16, 16), (tfd.W_FP8_ROW, 5)])
+def test_top1_confidence(wfmt, rows):
+    need_gpu()
+    case = make_case(20480, 4096, rows, wfmt, tid=380, tie_frac=0.01)
+    conf = torch.empty(rows, dtype=torch.float32, device="cuda")
+    y, tv, ti = tfd.tfd_head_gemv(case["w"], wfmt, case["scales"], case["x"], tfd.OUT_F32, topk=1,
+                                  top1_conf=conf)
+    torch.cuda.synchronize()
+    acc, S = oracle_acc_S(case, wfmt)
+    c = conf.cpu().numpy().astype(np.float64)
+    # against the confidence of the GPU's own fp32 logits: fp32 summation error only
+    assert np.allclose(c, top1_confidence(np32(y)), rtol=1e-4, atol=0)
+    # against the exact logits: each logit is within 1e-5 S, so the ratio within 2e-5 max S
+    tol = 2e-5 * S.max(axis=1) + 1e-4
+    assert np.all(np.abs(c - top1_confidence(acc)) <= tol * top1_confidence(acc))
+    # the confidence does not change the top-1
+    _, tv2, ti2 = tfd.tfd_head_gemv(case["w"], wfmt, case["scales"], case["x"], tfd.OUT_F32, topk=1)
+    torch.cuda.synchronize()
+    assert torch.equal(ti, ti2) and torch.equal(tv, tv2)
 
 
 def test_part_count_does_not_change_results():

@@ -74,3 +74,24 @@ def test_k_bounds():
         topk(np.zeros((1, 4), np.float32), 5)
     with pytest.raises(ValueError):
         topk(np.zeros((1, 4), np.float32), 0)
+
+
+def test_top1_confidence_closed_forms_and_softmax():
+    from scipy.special import softmax
+
+    from oracle.topk import top1_confidence
+    n = 1000
+    assert np.isclose(top1_confidence(np.zeros((1, n)))[0], 1.0 / n)
+    two = np.full((1, 10), -np.inf)
+    two[0, 3] = two[0, 7] = 2.5
+    assert top1_confidence(two)[0] == 0.5
+    lg = np.random.default_rng([0, 122, 0]).standard_normal((4, 5000)) * 3
+    ref = softmax(lg, axis=1).max(axis=1)
+    assert np.allclose(top1_confidence(lg), ref, rtol=1e-12)
+    assert np.allclose(top1_confidence(lg + 123.0), ref, rtol=1e-9)
+    withnan = lg.copy()
+    withnan[:, 10] = np.nan
+    withnan[:, 11] = -np.inf
+    assert np.allclose(top1_confidence(withnan),
+                       top1_confidence(np.delete(lg, [10, 11], axis=1)), rtol=1e-12)
+    assert np.isnan(top1_confidence(np.full((1, 3), np.nan))[0])

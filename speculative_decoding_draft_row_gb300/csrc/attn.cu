@@ -8,17 +8,24 @@
 // than the ring holds). Readings: half-split RoPE pairs (i, i + dim/2) turned by
 // p * base^(-2i/dim); the key is rounded to bf16 when written to the ring; the query stays fp32.
 //
-// One block per (head, stream): its 512 keys x 128 dims of K and V (256 KB) are read once with
-// 16-byte loads, half a warp per key row.
+// A cluster of 4 blocks per (head, stream) splits the window's keys; each block keeps its K and V
+// rows (128 keys x 256 B each) in flight at once, and the partial softmax states are combined in
+// distributed shared memory.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace {
 
 using namespace tfd;
+namespace cg = cooperative_groups;
 
 constexpr int kDim = 128;
 constexpr int kThreads = 256;
-constexpr int kMaxKeys = TFD_MAX_WINDOW + 1;
+constexpr int kCluster = 4;                       // blocks per (head, stream)
+constexpr int kMaxKeys = TFD_MAX_WINDOW + 1;      // 512
+constexpr int kKeysPerBlock = kMaxKeys / kCluster;  // 128
+constexpr int kKeysPerHalfWarp = kKeysPerBlock / 16;  // 8: 16 half-warps per block
 
 __device__ __forceinline__ float block_reduce(float v, float* sred, bool is_max) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -31,7 +38,9 @@ __device__ __forceinline__ float block_reduce(float v, float* sred, bool is_max)
   return r;
 }
 
-// Lane l of a warp holds elements 4l..4l+3 of a 128-vector: RMSNorm with gamma, then RoPE.
+// Lane l of a warp holds elements 4l..4l+3 of a 128-vector: RMSNorm with gamma, then RoPE. The
+// angle p * base^(-2i/dim) is formed and reduced modulo 2*pi in double, so the fp32 sine and
+// cosine stay accurate at large positions.
 __device__ __forceinline__ void norm_rope(float (&x)[4], const uint16_t* gamma, float eps, int p,
                                           float base) {
   const int lane = threadIdx.x & 31;
@@ -40,142 +49,160 @@ __device__ __forceinline__ void norm_rope(float (&x)[4], const uint16_t* gamma, 
   const float inv = 1.0f / sqrtf(ss / (float)kDim + eps);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    float gm = gamma ? bf16_bits_to_f32(gamma[4 * lane + j]) : 1.0f;
+    const float gm = gamma ? bf16_bits_to_f32(gamma[4 * lane + j]) : 1.0f;
     x[j] = x[j] * inv * gm;
   }
   float other[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) other[j] = __shfl_xor_sync(0xffffffffu, x[j], 16);
   const bool first_half = lane < 16;
+  const double lb = log2((double)base);
+  const double two_pi = 6.283185307179586476925286766559;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int i = 4 * (lane & 15) + j;  // pair index 0..63
-    const double ang = (double)p * pow((double)base, -2.0 * (double)i / (double)kDim);
-    double sd, cd;
-    sincos(ang, &sd, &cd);
-    const float c = (float)cd, s = (float)sd;
+    const double ang = (double)p * exp2(-2.0 * (double)i / (double)kDim * lb);
+    const float red = (float)(ang - two_pi * rint(ang / two_pi));
+    float s, c;
+    sincosf(red, &s, &c);
     // first half holds a = x[i] (partner b = x[i+64]); second half holds b (partner a).
     x[j] = first_half ? (x[j] * c - other[j] * s) : (other[j] * s + x[j] * c);
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
+struct AttnPartial {
+  float m, l;          // block max score and sum of exp(score - m)
+  float acc[kDim];     // sum of exp(score - m) * v
+};
+
+// Cluster of 4 blocks per (head, stream): block r of the cluster scores keys [128r, 128r + 128) of
+// the window with all their K and V rows in flight at once, keeps a softmax partial (max, sum,
+// weighted values), and block 0 combines the four partials read through distributed shared memory
+// in a fixed order. Block 0 also writes the new key/value row to the ring; every block computes
+// the current key itself, so no block reads the row another block writes.
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 window_attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k_new,
                    const uint16_t* __restrict__ v_new, const uint16_t* __restrict__ q_gamma,
                    const uint16_t* __restrict__ k_gamma, float eps, float rope_base,
                    const int32_t* __restrict__ pos, uint16_t* k_ring, uint16_t* v_ring, int ring,
                    int window, int heads, uint16_t* __restrict__ out, int32_t* dev_status) {
   __shared__ float qn[kDim];
-  __shared__ float scores[kMaxKeys];
+  __shared__ float kcur[kDim];
+  __shared__ float vcur[kDim];
+  __shared__ float scores[kKeysPerBlock];
   __shared__ float sred[kThreads / 32];
   __shared__ float red_o[16][kDim];
-  const int h = blockIdx.x, s = blockIdx.y;
+  __shared__ AttnPartial part;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = (int)cluster.block_rank();
+  const int h = blockIdx.x / kCluster, s = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int p = pos[s];
-  if (p < 0) {
-    if (tid == 0) set_dev_status(dev_status, TFD_ERR_DEVICE_DATA);
-    return;
-  }
-  const int slot = p % ring;
+  const bool bad = p < 0;  // uniform over the cluster: every block returns after the barriers
+  if (bad && crank == 0 && tid == 0) set_dev_status(dev_status, TFD_ERR_DEVICE_DATA);
+  const int pp = bad ? 0 : p;
+  const int slot = pp % ring;
   const int64_t head_off = ((int64_t)s * heads + h) * kDim;
   const int64_t ring_row = (((int64_t)s * ring + slot) * heads + h) * kDim;
+  const int p0 = pp - window > 0 ? pp - window : 0;
+  const int nk = pp - p0 + 1;
+  const int lo = crank * kKeysPerBlock;              // this block's keys: window index lo..hi-1
+  const int hi = lo + kKeysPerBlock < nk ? lo + kKeysPerBlock : nk;
+  const int hw = tid >> 4, hl = tid & 15;            // half-warp per key, 8 dims per lane
 
-  if (warp < 2) {
+  // issue this block's K and V rows (past positions only) before the prologue math
+  uint4 kv[kKeysPerHalfWarp], vv[kKeysPerHalfWarp];
+#pragma unroll
+  for (int u = 0; u < kKeysPerHalfWarp; ++u) {
+    const int i = lo + hw + 16 * u;
+    const bool past = !bad && i < hi && p0 + i < pp;
+    const int64_t row = (((int64_t)s * ring + (p0 + i) % ring) * heads + h) * kDim + hl * 8;
+    kv[u] = past ? *reinterpret_cast<const uint4*>(k_ring + row) : make_uint4(0u, 0u, 0u, 0u);
+    vv[u] = past ? *reinterpret_cast<const uint4*>(v_ring + row) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (!bad && warp < 2) {
     const uint16_t* src = (warp == 0 ? q : k_new) + head_off + 4 * lane;
     uint2 raw = *reinterpret_cast<const uint2*>(src);
     float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    norm_rope(x, warp == 0 ? q_gamma : k_gamma, eps, p, rope_base);
+    norm_rope(x, warp == 0 ? q_gamma : k_gamma, eps, pp, rope_base);
     if (warp == 0) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) qn[4 * lane + j] = x[j];
     } else {
-      uint2 o;
-      o.x = f32_to_bf16_bits(x[0]) | ((uint32_t)f32_to_bf16_bits(x[1]) << 16);
-      o.y = f32_to_bf16_bits(x[2]) | ((uint32_t)f32_to_bf16_bits(x[3]) << 16);
-      *reinterpret_cast<uint2*>(k_ring + ring_row + 4 * lane) = o;
+      uint16_t b[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) { b[j] = f32_to_bf16_bits(x[j]); kcur[4 * lane + j] = bf16_bits_to_f32(b[j]); }
+      if (crank == 0) {
+        uint2 o;
+        o.x = b[0] | ((uint32_t)b[1] << 16);
+        o.y = b[2] | ((uint32_t)b[3] << 16);
+        *reinterpret_cast<uint2*>(k_ring + ring_row + 4 * lane) = o;
+      }
     }
-  } else if (warp == 2) {
-    *reinterpret_cast<uint2*>(v_ring + ring_row + 4 * lane) =
-        *reinterpret_cast<const uint2*>(v_new + head_off + 4 * lane);
+  } else if (!bad && warp == 2) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(v_new + head_off + 4 * lane);
+    vcur[4 * lane] = bf16_lo(raw.x);
+    vcur[4 * lane + 1] = bf16_hi(raw.x);
+    vcur[4 * lane + 2] = bf16_lo(raw.y);
+    vcur[4 * lane + 3] = bf16_hi(raw.y);
+    if (crank == 0) *reinterpret_cast<uint2*>(v_ring + ring_row + 4 * lane) = raw;
   }
   __syncthreads();
 
-  const int p0 = p - window > 0 ? p - window : 0;
-  const int nk = p - p0 + 1;
-  const int hw = tid >> 4, hl = tid & 15;  // half-warp per key, 8 dims per lane
+  // scores of this block's keys (the current key from registers of the prologue, via kcur)
   float qv[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) qv[j] = qn[hl * 8 + j];
   const float inv_sqrt_d = 1.0f / sqrtf((float)kDim);
-  // Trip counts depend on nk only, so both halves of a warp run the same iterations (the
-  // half-warp shuffles below need the whole warp).
-  for (int ib = 0; ib < nk; ib += 16 * 4) {
-    const int i0 = ib + hw;
-    uint4 kv[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + 16 * u;
-      if (i < nk) {
-        const int sl = (p0 + i) % ring;
-        kv[u] = *reinterpret_cast<const uint4*>(
-            k_ring + (((int64_t)s * ring + sl) * heads + h) * kDim + hl * 8);
-      } else {
-        kv[u] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
+  for (int u = 0; u < kKeysPerHalfWarp; ++u) {
+    const int i = lo + hw + 16 * u;
+    float d = 0.0f;
+    if (!bad && i < hi && p0 + i == pp) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      uint32_t w[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-      float d = 0.0f;
+      for (int j = 0; j < 8; ++j) d = fmaf(qv[j], kcur[hl * 8 + j], d);
+    } else {
+      const uint32_t w[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         d = fmaf(qv[2 * j], bf16_lo(w[j]), d);
         d = fmaf(qv[2 * j + 1], bf16_hi(w[j]), d);
       }
-#pragma unroll
-      for (int m = 8; m > 0; m >>= 1) d += __shfl_xor_sync(0xffffffffu, d, m);
-      const int i = i0 + 16 * u;
-      if (hl == 0 && i < nk) scores[i] = d * inv_sqrt_d;
     }
+#pragma unroll
+    for (int m = 8; m > 0; m >>= 1) d += __shfl_xor_sync(0xffffffffu, d, m);
+    if (hl == 0 && i < hi) scores[i - lo] = d * inv_sqrt_d;
   }
   __syncthreads();
+  const int nb = hi > lo ? hi - lo : 0;
   float mx = -INFINITY;
-  for (int i = tid; i < nk; i += kThreads) mx = fmaxf(mx, scores[i]);
+  for (int i = tid; i < nb; i += kThreads) mx = fmaxf(mx, scores[i]);
   mx = block_reduce(mx, sred, true);
   float sum = 0.0f;
-  for (int i = tid; i < nk; i += kThreads) {
-    float e = expf(scores[i] - mx);
+  for (int i = tid; i < nb; i += kThreads) {
+    const float e = expf(scores[i] - mx);
     scores[i] = e;
     sum += e;
   }
-  sum = block_reduce(sum, sred, false);  // its first barrier also publishes scores[]
-
+  sum = block_reduce(sum, sred, false);  // its barriers also publish scores[]
   float acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-  for (int ib = 0; ib < nk; ib += 16 * 4) {
-    const int i0 = ib + hw;
-    uint4 vv[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + 16 * u;
-      if (i < nk) {
-        const int sl = (p0 + i) % ring;
-        vv[u] = *reinterpret_cast<const uint4*>(
-            v_ring + (((int64_t)s * ring + sl) * heads + h) * kDim + hl * 8);
+  for (int u = 0; u < kKeysPerHalfWarp; ++u) {
+    const int i = lo + hw + 16 * u;
+    if (i < hi) {
+      const float e = scores[i - lo];
+      if (p0 + i == pp) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(e, vcur[hl * 8 + j], acc[j]);
       } else {
-        vv[u] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
+        const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + 16 * u;
-      const float e = i < nk ? scores[i] : 0.0f;
-      uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc[2 * j] = fmaf(e, bf16_lo(w[j]), acc[2 * j]);
-        acc[2 * j + 1] = fmaf(e, bf16_hi(w[j]), acc[2 * j + 1]);
+        for (int j = 0; j < 4; ++j) {
+          acc[2 * j] = fmaf(e, bf16_lo(w[j]), acc[2 * j]);
+          acc[2 * j + 1] = fmaf(e, bf16_hi(w[j]), acc[2 * j + 1]);
+        }
       }
     }
   }
@@ -185,8 +212,24 @@ window_attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ 
   if (tid < kDim) {
     float o = 0.0f;
     for (int g = 0; g < 16; ++g) o += red_o[g][tid];
-    out[((int64_t)s * heads + h) * kDim + tid] = f32_to_bf16_bits(o / sum);
+    part.acc[tid] = o;
   }
+  if (tid == 0) { part.m = mx; part.l = sum; }
+  cluster.sync();  // every block's partial is written
+  if (crank == 0 && !bad && tid < kDim) {
+    float mm = -INFINITY;
+    for (int r = 0; r < kCluster; ++r) mm = fmaxf(mm, cluster.map_shared_rank(&part, r)->m);
+    float l = 0.0f, o = 0.0f;
+    for (int r = 0; r < kCluster; ++r) {
+      const AttnPartial* pr = cluster.map_shared_rank(&part, r);
+      if (pr->m == -INFINITY) continue;  // a block with no keys
+      const float f = expf(pr->m - mm);
+      l += pr->l * f;
+      o += pr->acc[tid] * f;
+    }
+    out[head_off + tid] = f32_to_bf16_bits(o / l);
+  }
+  cluster.sync();  // keep every block's shared memory alive until block 0 has read it
 }
 
 }  // namespace
@@ -206,7 +249,8 @@ extern "C" tfd_status tfd_window_attn(const void* q, const void* k_new, const vo
       !aligned(v_ring, 16) || !aligned(out, 16) || !aligned(pos, 4))
     return TFD_ERR_INVALID;
   if ((q_gamma && !aligned(q_gamma, 2)) || (k_gamma && !aligned(k_gamma, 2))) return TFD_ERR_INVALID;
-  dim3 grid(heads, streams);
+  if ((int64_t)heads * 4 > 2147483647) return TFD_ERR_INVALID;
+  dim3 grid(heads * 4, streams);
   window_attn_kernel<<<grid, kThreads, 0, tfd_host::as_stream(stream)>>>(
       reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint16_t*>(k_new),
       reinterpret_cast<const uint16_t*>(v_new), reinterpret_cast<const uint16_t*>(q_gamma),

@@ -37,7 +37,7 @@ namespace {
 #define TFD_GEMV_DEPTH_FP8_NT2 8
 #endif
 #ifndef TFD_GEMV_DEPTH_BLK_NT2
-#define TFD_GEMV_DEPTH_BLK_NT2 8
+#define TFD_GEMV_DEPTH_BLK_NT2 4
 #endif
 // Minimum resident blocks per SM asked of the compiler for one n-tile (2 caps registers at 64).
 #ifndef TFD_GEMV_MINB_NT1

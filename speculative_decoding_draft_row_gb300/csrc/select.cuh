@@ -173,7 +173,18 @@ __device__ inline void rank_count_select(const uint64_t* c, int n, int k, uint64
     const uint64_t a = c[i0];
     const uint64_t b = i1 < n ? c[i1] : 0ull;
     int ra = 0, rb = 0;
-    for (int j = 0; j < n; ++j) {
+    int j = 0;
+    for (; j + 8 <= n; j += 8) {  // 8 independent broadcast loads in flight
+      uint64_t x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = c[j + u];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        ra += (x[u] > a) | ((x[u] == a) & (j + u < i0));
+        rb += (x[u] > b) | ((x[u] == b) & (j + u < i1));
+      }
+    }
+    for (; j < n; ++j) {
       const uint64_t x = c[j];
       ra += (x > a) | ((x == a) & (j < i0));
       rb += (x > b) | ((x == b) & (j < i1));
@@ -227,17 +238,26 @@ __device__ inline void block_topk_fast(int cnt, int k, const uint64_t* keys, uin
   }
   __syncthreads();
   const uint64_t bstar = (uint64_t)fs.bstar;
+  // gather the keys at or above the boundary bin: each warp counts its takers with ballots,
+  // reserves its slots with one atomic, then writes them in order
   const int rounds = (cnt + kSelectThreads - 1) / kSelectThreads;
-  for (int r = 0; r < rounds; ++r) {  // whole warps iterate together for the ballot
+  int wcount = 0;
+  for (int r = 0; r < rounds; ++r) {
+    const int i = r * kSelectThreads + tid;
+    const bool take = i < cnt && (keys[i] >> (64 - kDigitBits)) >= bstar;
+    wcount += __popc(__ballot_sync(0xffffffffu, take));
+  }
+  int base = 0;
+  if (lane == 0) base = atomicAdd(&fs.n_cand, wcount);
+  base = __shfl_sync(0xffffffffu, base, 0);
+  for (int r = 0; r < rounds; ++r) {
     const int i = r * kSelectThreads + tid;
     const uint64_t key = i < cnt ? keys[i] : 0ull;
     const bool take = i < cnt && (key >> (64 - kDigitBits)) >= bstar;
     const unsigned m = __ballot_sync(0xffffffffu, take);
-    int base = 0;
-    if (lane == 0 && m) base = atomicAdd(&fs.n_cand, __popc(m));
-    base = __shfl_sync(0xffffffffu, base, 0);
     const int at = base + __popc(m & ((1u << lane) - 1u));
     if (take && at < kCandCap) fs.cand[at] = key;
+    base += __popc(m);
   }
   __syncthreads();
   const int ncand = fs.n_cand;

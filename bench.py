@@ -219,6 +219,35 @@ def time_calls(fn, iters, stream):
     return a.elapsed_time(b) / iters
 
 
+def time_graph(fn, iters, per_graph=10):
+    """Mean device time of fn() in ms with the host out of the way: per_graph calls captured in one
+    CUDA graph, replayed until about iters calls ran (CUDA events on the replaying stream)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            fn()
+    reps = max(1, iters // per_graph)
+    for _ in range(2):
+        g.replay()
+    stream = torch.cuda.current_stream()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / (reps * per_graph)
+
+
 def run_ours(args):
     import torch
 
@@ -326,7 +355,7 @@ def run_ours(args):
                                           top_vals=v64, top_ids=i64, ws=ws64)
             for _ in range(3):
                 f()
-            ms = time_calls(f, 20, stream)
+            ms = time_graph(f, 20)
             gbs = fp8_call_bytes(r) / (ms * 1e-3) / 1e9
             out[str(r)] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
                            "frac": round(gbs / peak, 4)}
@@ -424,12 +453,14 @@ def measure_rows_of_path(wd, stream, peak):
     out = {}
 
     def rec(name, fn, nbytes, reps=20):
+        # device time from graph replays; eager calls add the host's launch overhead
         for _ in range(3):
             fn()
-        ms = time_calls(fn, reps, stream)
+        ms_eager = time_calls(fn, reps, stream)
+        ms = time_graph(fn, reps)
         gbs = nbytes / (ms * 1e-3) / 1e9
-        out[name] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                     "bytes": nbytes}
+        out[name] = {"us": round(ms * 1e3, 2), "us_eager": round(ms_eager * 1e3, 2),
+                     "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nbytes}
 
     # two-stage head, 16 rows: B x, A h, top cand_k of the low-rank logits, exact rescore
     a, b = inputs.low_rank()
@@ -440,15 +471,15 @@ def measure_rows_of_path(wd, stream, peak):
     for ck in (1, 64, 512):
         cv = torch.empty((16, ck), dtype=torch.float32, device="cuda")
         ci = torch.empty((16, ck), dtype=torch.int32, device="cuda")
-        tws = tfd.zeroed_workspace(tfd.tfd_topk_workspace(16, VOCAB, ck))
+        tws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(16, VOCAB, ck, 0))
         rws = tfd.zeroed_workspace(tfd.tfd_rescore_workspace(16, ck))
         oi = torch.empty(16, dtype=torch.int32, device="cuda")
         ov = torch.empty(16, dtype=torch.float32, device="cuda")
 
         def two_stage():
             tfd.tfd_head_gemv(bd, tfd.W_BF16, None, x16, tfd.OUT_F32, y=h)
-            tfd.tfd_head_gemv(ad, tfd.W_BF16, None, h, tfd.OUT_F32, y=z)
-            tfd.tfd_topk(z, ck, vals=cv, ids=ci, ws=tws)
+            tfd.tfd_head_gemv(ad, tfd.W_BF16, None, h, tfd.OUT_F32, y=z, topk=ck, top_vals=cv,
+                              top_ids=ci, ws=tws)
             tfd.tfd_rescore(wd, x16, ci, out_ids=oi, out_vals=ov, ws=rws, want_logits=False)
 
         # what the method must move: B, A, the activations and the gathered exact-head rows
@@ -503,7 +534,7 @@ def run_fp8_case(args):
                                       top_vals=v, top_ids=i, ws=ws)
         for _ in range(args.warmup):
             f()
-        ms = time_calls(f, args.steps, stream)
+        ms = time_graph(f, args.steps)
         out[str(r)] = {"us": round(ms * 1e3, 2),
                        "gbs": round(fp8_call_bytes(r) / (ms * 1e-3) / 1e9, 1)}
     print(json.dumps({"case": f"fp8 {args.fp8} top-64", "per_rows": out}), flush=True)
@@ -527,14 +558,15 @@ def run_case(args):
         out = torch.empty((PASS_STREAMS, PASS_HEADS * PASS_DIM), dtype=torch.bfloat16,
                           device="cuda")
         fn = lambda: tfd.tfd_window_attn(q, k, v, pos, krd, vrd, PASS_WINDOW, out=out)
-    elif c in ("rescore", "topk512", "twostage"):
+    elif c in ("rescore", "topk64", "topk512", "twostage"):
         x16 = inputs.rows(16).cuda()
-        if c == "topk512":
+        if c.startswith("topk"):
+            kk = int(c[4:])
             z = torch.from_numpy(inputs.normal_f32((16, VOCAB), 1.0, 90)).cuda()
-            ws = tfd.zeroed_workspace(tfd.tfd_topk_workspace(16, VOCAB, 512))
-            cv = torch.empty((16, 512), dtype=torch.float32, device="cuda")
-            ci = torch.empty((16, 512), dtype=torch.int32, device="cuda")
-            fn = lambda: tfd.tfd_topk(z, 512, vals=cv, ids=ci, ws=ws)
+            ws = tfd.zeroed_workspace(tfd.tfd_topk_workspace(16, VOCAB, kk))
+            cv = torch.empty((16, kk), dtype=torch.float32, device="cuda")
+            ci = torch.empty((16, kk), dtype=torch.int32, device="cuda")
+            fn = lambda: tfd.tfd_topk(z, kk, vals=cv, ids=ci, ws=ws)
         else:
             w, _ = inputs.head(tie_frac=0.01)
             wd = w.cuda()
@@ -552,22 +584,24 @@ def run_case(args):
                 ad, bd = a.cuda(), b.cuda()
                 h = torch.empty((16, 256), dtype=torch.float32, device="cuda")
                 z = torch.empty((16, VOCAB), dtype=torch.float32, device="cuda")
-                tws = tfd.zeroed_workspace(tfd.tfd_topk_workspace(16, VOCAB, 512))
+                tws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(16, VOCAB, 512, 0))
                 cv = torch.empty((16, 512), dtype=torch.float32, device="cuda")
                 ci = torch.empty((16, 512), dtype=torch.int32, device="cuda")
 
                 def fn():
                     tfd.tfd_head_gemv(bd, tfd.W_BF16, None, x16, tfd.OUT_F32, y=h)
-                    tfd.tfd_head_gemv(ad, tfd.W_BF16, None, h, tfd.OUT_F32, y=z)
-                    tfd.tfd_topk(z, 512, vals=cv, ids=ci, ws=tws)
+                    tfd.tfd_head_gemv(ad, tfd.W_BF16, None, h, tfd.OUT_F32, y=z, topk=512,
+                                      top_vals=cv, top_ids=ci, ws=tws)
                     tfd.tfd_rescore(wd, x16, ci, out_ids=oi, out_vals=ov, ws=rws,
                                     want_logits=False)
     else:
         raise SystemExit(f"unknown case {c}")
     for _ in range(args.warmup):
         fn()
-    ms = time_calls(fn, args.steps, stream)
-    print(json.dumps({"case": c, "us": round(ms * 1e3, 2)}), flush=True)
+    ms_eager = time_calls(fn, args.steps, stream)
+    ms = time_graph(fn, args.steps)
+    print(json.dumps({"case": c, "us": round(ms * 1e3, 2), "us_eager": round(ms_eager * 1e3, 2)}),
+          flush=True)
 
 
 def run_reference(args):
@@ -611,7 +645,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", choices=["row", "block32"], default=None,
                     help="profiling case: only the FP8 head with fused top-64")
-    ap.add_argument("--case", choices=["attn", "rescore", "topk512", "twostage"], default=None,
+    ap.add_argument("--case", choices=["attn", "rescore", "topk64", "topk512", "twostage"],
+                    default=None,
                     help="profiling case: one row of the path alone")
     ap.add_argument("--no-extras", action="store_true",
                     help="time the headline calls only (no e2e, FP8 or CPU baseline): a small "

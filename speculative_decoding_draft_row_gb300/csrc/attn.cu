@@ -8,10 +8,12 @@
 // than the ring holds). Readings: half-split RoPE pairs (i, i + dim/2) turned by
 // p * base^(-2i/dim); the key is rounded to bf16 when written to the ring; the query stays fp32.
 //
-// A cluster of 4 blocks per (head, stream) splits the window's keys; each block keeps its K and V
-// rows (128 keys x 256 B each) in flight at once, and the partial softmax states are combined in
-// distributed shared memory.
+// A cluster of 4 blocks per (head, stream) splits the window's keys; each block keeps its K rows
+// (in registers) and V rows (asynchronous copies into shared memory) in flight at once, 128 keys
+// x 256 B each, and the partial softmax states are combined in distributed shared memory.
 #include <cooperative_groups.h>
+
+#include <cmath>
 
 #include "common.cuh"
 
@@ -38,11 +40,18 @@ __device__ __forceinline__ float block_reduce(float v, float* sred, bool is_max)
   return r;
 }
 
-// Lane l of a warp holds elements 4l..4l+3 of a 128-vector: RMSNorm with gamma, then RoPE. The
-// angle p * base^(-2i/dim) is formed and reduced modulo 2*pi in double, so the fp32 sine and
-// cosine stay accurate at large positions.
+// Each pair's frequency base^(-2i/dim) in turns (1 turn = 2 pi), as a 64-bit binary fraction:
+// t_i = frac(base^(-2i/dim) / (2 pi)) * 2^64. For an integer position p, p * t_i mod 2^64 is the
+// angle p * base^(-2i/dim) reduced to one turn, exact up to the rounding of t_i (2^-53 relative),
+// so the reduction needs no floating-point arithmetic on the device.
+struct RopeTurns {
+  uint64_t t[kDim / 2];
+};
+
+// Lane l of a warp holds elements 4l..4l+3 of a 128-vector: RMSNorm with gamma, then RoPE with
+// the angle reduced to [-pi, pi) before the fp32 sine and cosine.
 __device__ __forceinline__ void norm_rope(float (&x)[4], const uint16_t* gamma, float eps, int p,
-                                          float base) {
+                                          const RopeTurns& turns) {
   const int lane = threadIdx.x & 31;
   float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
   ss = warp_sum(ss);
@@ -56,13 +65,12 @@ __device__ __forceinline__ void norm_rope(float (&x)[4], const uint16_t* gamma, 
 #pragma unroll
   for (int j = 0; j < 4; ++j) other[j] = __shfl_xor_sync(0xffffffffu, x[j], 16);
   const bool first_half = lane < 16;
-  const double lb = log2((double)base);
-  const double two_pi = 6.283185307179586476925286766559;
+  const float turn_unit = 1.4629180792671596e-9f;  // 2 pi / 2^32
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int i = 4 * (lane & 15) + j;  // pair index 0..63
-    const double ang = (double)p * exp2(-2.0 * (double)i / (double)kDim * lb);
-    const float red = (float)(ang - two_pi * rint(ang / two_pi));
+    const uint64_t ph = (uint64_t)(uint32_t)p * turns.t[i];  // mod 2^64: the reduced angle
+    const float red = (float)(int32_t)(ph >> 32) * turn_unit;
     float s, c;
     sincosf(red, &s, &c);
     // first half holds a = x[i] (partner b = x[i+64]); second half holds b (partner a).
@@ -80,10 +88,10 @@ struct AttnPartial {
 // weighted values), and block 0 combines the four partials read through distributed shared memory
 // in a fixed order. Block 0 also writes the new key/value row to the ring; every block computes
 // the current key itself, so no block reads the row another block writes.
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 4)
 window_attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k_new,
                    const uint16_t* __restrict__ v_new, const uint16_t* __restrict__ q_gamma,
-                   const uint16_t* __restrict__ k_gamma, float eps, float rope_base,
+                   const uint16_t* __restrict__ k_gamma, float eps, const RopeTurns turns,
                    const int32_t* __restrict__ pos, uint16_t* k_ring, uint16_t* v_ring, int ring,
                    int window, int heads, uint16_t* __restrict__ out, int32_t* dev_status) {
   __shared__ float qn[kDim];
@@ -93,6 +101,7 @@ window_attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ 
   __shared__ float sred[kThreads / 32];
   __shared__ float red_o[16][kDim];
   __shared__ AttnPartial part;
+  __shared__ __align__(16) uint16_t vsm[kKeysPerBlock][kDim];  // V rows, copied asynchronously
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
   const int h = blockIdx.x / kCluster, s = blockIdx.y;
@@ -110,21 +119,28 @@ window_attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ 
   const int hi = lo + kKeysPerBlock < nk ? lo + kKeysPerBlock : nk;
   const int hw = tid >> 4, hl = tid & 15;            // half-warp per key, 8 dims per lane
 
-  // issue this block's K and V rows (past positions only) before the prologue math
-  uint4 kv[kKeysPerHalfWarp], vv[kKeysPerHalfWarp];
+  // issue this block's K rows (into registers) and V rows (asynchronous copies into shared
+  // memory, zero-filled for rows that are not past positions) before the prologue math; each
+  // thread later reads back only the V bytes it copied itself
+  uint4 kv[kKeysPerHalfWarp];
 #pragma unroll
   for (int u = 0; u < kKeysPerHalfWarp; ++u) {
     const int i = lo + hw + 16 * u;
     const bool past = !bad && i < hi && p0 + i < pp;
     const int64_t row = (((int64_t)s * ring + (p0 + i) % ring) * heads + h) * kDim + hl * 8;
     kv[u] = past ? *reinterpret_cast<const uint4*>(k_ring + row) : make_uint4(0u, 0u, 0u, 0u);
-    vv[u] = past ? *reinterpret_cast<const uint4*>(v_ring + row) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&vsm[hw + 16 * u][hl * 8]);
+    const uint16_t* src = past ? v_ring + row : v_ring;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(past ? 16 : 0)
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
   if (!bad && warp < 2) {
     const uint16_t* src = (warp == 0 ? q : k_new) + head_off + 4 * lane;
     uint2 raw = *reinterpret_cast<const uint2*>(src);
     float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    norm_rope(x, warp == 0 ? q_gamma : k_gamma, eps, pp, rope_base);
+    norm_rope(x, warp == 0 ? q_gamma : k_gamma, eps, pp, turns);
     if (warp == 0) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) qn[4 * lane + j] = x[j];
@@ -185,6 +201,7 @@ window_attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ 
     sum += e;
   }
   sum = block_reduce(sum, sred, false);  // its barriers also publish scores[]
+  asm volatile("cp.async.wait_group 0;" ::: "memory");  // this thread's V copies have landed
   float acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
@@ -197,7 +214,8 @@ window_attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ 
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = fmaf(e, vcur[hl * 8 + j], acc[j]);
       } else {
-        const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+        const uint4 vq = *reinterpret_cast<const uint4*>(&vsm[hw + 16 * u][hl * 8]);
+        const uint32_t w[4] = {vq.x, vq.y, vq.z, vq.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           acc[2 * j] = fmaf(e, bf16_lo(w[j]), acc[2 * j]);
@@ -232,6 +250,24 @@ window_attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ 
   cluster.sync();  // keep every block's shared memory alive until block 0 has read it
 }
 
+// The turn table of a RoPE base, computed in double on the host (kept for the last base used by
+// this thread).
+const RopeTurns& rope_turns(float base) {
+  thread_local float cached_base = -1.0f;
+  thread_local RopeTurns cached;
+  if (cached_base != base) {
+    const double two_pi = 6.283185307179586476925286766559;
+    for (int i = 0; i < kDim / 2; ++i) {
+      const double f = std::pow((double)base, -2.0 * i / kDim);
+      double turns = f / two_pi;
+      turns -= std::floor(turns);
+      cached.t[i] = (uint64_t)std::ldexp(turns, 64);
+    }
+    cached_base = base;
+  }
+  return cached;
+}
+
 }  // namespace
 
 extern "C" tfd_status tfd_window_attn(const void* q, const void* k_new, const void* v_new,
@@ -254,7 +290,7 @@ extern "C" tfd_status tfd_window_attn(const void* q, const void* k_new, const vo
   window_attn_kernel<<<grid, kThreads, 0, tfd_host::as_stream(stream)>>>(
       reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint16_t*>(k_new),
       reinterpret_cast<const uint16_t*>(v_new), reinterpret_cast<const uint16_t*>(q_gamma),
-      reinterpret_cast<const uint16_t*>(k_gamma), eps, rope_base, pos,
+      reinterpret_cast<const uint16_t*>(k_gamma), eps, rope_turns(rope_base), pos,
       reinterpret_cast<uint16_t*>(k_ring), reinterpret_cast<uint16_t*>(v_ring), ring, window,
       heads, reinterpret_cast<uint16_t*>(out), dev_status);
   return tfd_host::launch_status();

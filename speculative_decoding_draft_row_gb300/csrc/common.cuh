@@ -123,7 +123,8 @@ inline int sm_count() {
 
 // Internal launchers shared across translation units.
 namespace tfd_internal {
-// Split top-k over fp32 logits (see topk.cu). The workspace is tfd_topk_workspace() bytes.
+// Top-k over fp32 logits by a threshold filter, one thread-block cluster per row (topk.cu). The
+// workspace is tfd_topk_workspace() bytes.
 tfd_status topk_launch(const float* logits, int rows, int64_t n, int64_t ld, int k,
                        const int32_t* id_map, float* vals, int32_t* ids, int64_t ld_out, void* ws,
                        size_t ws_bytes, cudaStream_t stream);

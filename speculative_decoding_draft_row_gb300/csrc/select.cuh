@@ -270,4 +270,21 @@ __device__ inline void block_topk_fast(int cnt, int k, const uint64_t* keys, uin
   rank_count_select(fs.cand, ncand, k, out);
 }
 
+// Sorts a[0..np) descending in shared memory by a bitonic network (np a power of two). Called by
+// all kSelectThreads threads of the block; returns after a barrier.
+__device__ inline void block_sort_desc(uint64_t* a, int np) {
+  const int tid = threadIdx.x;
+  __syncthreads();
+  for (int size = 2; size <= np; size <<= 1) {
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      for (int t = tid; t < (np >> 1); t += kSelectThreads) {
+        const int i = 2 * t - (t & (j - 1));
+        const uint64_t x = a[i], y = a[i + j];
+        if (((i & size) == 0) ? (x < y) : (x > y)) { a[i] = y; a[i + j] = x; }
+      }
+      __syncthreads();
+    }
+  }
+}
+
 }  // namespace tfd

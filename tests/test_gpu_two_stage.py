@@ -18,8 +18,11 @@ def two_stage_gpu(a, b, w, x, cand_k):
     h, _, _ = tfd.tfd_head_gemv(b, tfd.W_BF16, None, x, tfd.OUT_F32)
     z, _, _ = tfd.tfd_head_gemv(a, tfd.W_BF16, None, h, tfd.OUT_F32)
     cv, ci = tfd.tfd_topk(z, cand_k)
+    # the same candidates from the GEMV with its fused top-k (sub-group maxima from its epilogue)
+    _, fv, fi = tfd.tfd_head_gemv(a, tfd.W_BF16, None, h, tfd.OUT_NONE, topk=cand_k)
     e, ids, vals = tfd.tfd_rescore(w, x, ci)
     torch.cuda.synchronize()
+    assert torch.equal(fi, ci) and same_bits(np32(fv), np32(cv)), "fused top-k != top-k of z"
     return h, z, cv, ci, e, ids, vals
 
 

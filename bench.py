@@ -495,6 +495,24 @@ def measure_rows_of_path(wd, stream, peak):
     rec("window_attn_4x32_w511",
         lambda: tfd.tfd_window_attn(q, k, v, pos, krd, vrd, PASS_WINDOW, out=att),
         PASS_STREAMS * PASS_HEADS * (PASS_WINDOW + 1) * PASS_DIM * 2 * 2)
+    # the rest of the head layer: RMSNorm of the hidden rows, SwiGLU, a 128-row prompt-chunk absorb
+    hid = torch.from_numpy(inputs.normal_f32((PASS_STREAMS, HIDDEN), 1.0, 61)).to(torch.bfloat16).cuda()
+    hout = torch.empty_like(hid)
+    gam = torch.ones(HIDDEN, dtype=torch.bfloat16, device="cuda")
+    rec("rmsnorm_4x4096", lambda: tfd.tfd_rmsnorm(hid, gam, 1e-6, out=hout),
+        PASS_STREAMS * HIDDEN * 2 * 2 + HIDDEN * 2)
+    gg = torch.from_numpy(inputs.normal_f32((PASS_STREAMS, HIDDEN_FFN), 1.0, 62)).to(torch.bfloat16).cuda()
+    uu = torch.from_numpy(inputs.normal_f32((PASS_STREAMS, HIDDEN_FFN), 1.0, 63)).to(torch.bfloat16).cuda()
+    so = torch.empty_like(gg)
+    rec("swiglu_4x11008", lambda: tfd.tfd_swiglu(gg, uu, out=so), PASS_STREAMS * HIDDEN_FFN * 2 * 3)
+    nab = 128
+    kab = torch.from_numpy(inputs.normal_f32((PASS_STREAMS * nab * PASS_HEADS, PASS_DIM), 1.0, 64)).to(
+        torch.bfloat16).cuda().reshape(PASS_STREAMS, nab, PASS_HEADS, PASS_DIM)
+    vab = torch.from_numpy(inputs.normal_f32((PASS_STREAMS * nab * PASS_HEADS, PASS_DIM), 1.0, 65)).to(
+        torch.bfloat16).cuda().reshape(PASS_STREAMS, nab, PASS_HEADS, PASS_DIM)
+    p0 = torch.zeros(PASS_STREAMS, dtype=torch.int32, device="cuda")
+    rec("absorb_4x128rows", lambda: tfd.tfd_absorb(kab, vab, p0, krd, vrd),
+        PASS_STREAMS * nab * PASS_HEADS * PASS_DIM * 2 * 4)
     # accept of a 5-draft window over 4 streams
     dr = torch.arange(20, dtype=torch.int32, device="cuda").reshape(4, 5)
     na = torch.full((4,), 5, dtype=torch.int32, device="cuda")
@@ -524,10 +542,11 @@ def run_fp8_case(args):
     mode = tfd.W_FP8_ROW if args.fp8 == "row" else tfd.W_FP8_BLOCK32
     w, _ = inputs.head(tie_frac=0.01)
     codes, scales = tfd.tfd_quant_fp8(w.cuda(), mode)
-    xs = {r: inputs.rows(16)[:r].cuda() for r in ROWS}
+    row_counts = ROWS if args.rows is None else [args.rows]
+    xs = {r: inputs.rows(16)[:r].cuda() for r in row_counts}
     ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(16, VOCAB, 64))
     out = {}
-    for r in ROWS:
+    for r in row_counts:
         v = torch.empty((r, 64), dtype=torch.float32, device="cuda")
         i = torch.empty((r, 64), dtype=torch.int32, device="cuda")
         f = lambda: tfd.tfd_head_gemv(codes, mode, scales, xs[r], tfd.OUT_NONE, topk=64,
@@ -645,6 +664,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", choices=["row", "block32"], default=None,
                     help="profiling case: only the FP8 head with fused top-64")
+    ap.add_argument("--rows", type=int, default=None, choices=list(range(1, 17)),
+                    help="with --fp8: one row count instead of 1/5/10/15")
     ap.add_argument("--case", choices=["attn", "rescore", "topk64", "topk512", "twostage"],
                     default=None,
                     help="profiling case: one row of the path alone")

@@ -237,6 +237,49 @@ tfd_status tfd_accept(const int32_t* drafts, const int32_t* n_asked, const int32
                       int streams, int win, int32_t* n_kept, int64_t* asked_hist,
                       int64_t* kept_hist, int32_t* dev_status, void* stream);
 
+/*
+ * tfd_rmsnorm - RMSNorm of hidden rows.
+ *   [TFE] eagle.cu's row kernels include RMSNorm; qk_norm is the same normalisation per head.
+ *   out[r][i] = bf16(x[r][i] / sqrt(mean_i(x[r][i]^2) + eps) * gamma[i]), sums in fp32.
+ * Args:
+ *   x device bf16 [rows][ldx]; out device bf16 [rows][ldo] (may equal x: in place);
+ *   gamma device bf16 [hidden] or NULL (ones); rows >= 1; hidden >= 8 and hidden % 8 == 0;
+ *   ldx, ldo >= hidden and multiples of 8; eps >= 0; x, out, gamma 16-byte aligned.
+ */
+tfd_status tfd_rmsnorm(const void* x, int64_t ldx, const void* gamma, float eps, int rows,
+                       int64_t hidden, void* out, int64_t ldo, void* stream);
+
+/*
+ * tfd_swiglu - SwiGLU of a gate and an up row, SiLU rounded to bf16 before the multiply.
+ *   [TFE] the reference "rounds SiLU(g) to bf16 before the multiply", as the silu-mul row kernel
+ *   does. out = bf16(bf16(SiLU(g)) * u), SiLU(g) = g / (1 + exp(-g)) in fp32.
+ * Args:
+ *   g, u device bf16 [rows][ld]; out device bf16 [rows][ldo] (may equal g or u); rows >= 1;
+ *   cols >= 8 and cols % 8 == 0; ld, ldo >= cols and multiples of 8; 16-byte aligned.
+ */
+tfd_status tfd_swiglu(const void* g, const void* u, int64_t ld, int rows, int64_t cols, void* out,
+                      int64_t ldo, void* stream);
+
+/*
+ * tfd_absorb - write a span of key/value rows into each stream's ring (a prompt chunk or a round).
+ *   [TFE] first commits: an absorb of more rows than the ring wrote two rows to one ring row, and
+ *   "absorb refuses a larger span"; commit "... ocabulary head": qk_norm before RoPE, and a prompt
+ *   chunk gives the head its last ring of rows.
+ *   For stream s and row i < n at position p = p0[s] + i:
+ *     k_ring[s][p % ring][h] = bf16(rope(rmsnorm(k_rows[s][i][h]) * k_gamma, p));
+ *     v_ring[s][p % ring][h] = v_rows[s][i][h];
+ *   with the normalisation and rotation of tfd_window_attn.
+ * Args:
+ *   k_rows, v_rows device bf16 [streams][n][heads][dim]; k_gamma device bf16 [dim] or NULL;
+ *   p0 device int32 [streams] (negative, or p0 + n past INT32_MAX: TFD_ERR_DEVICE_DATA and that
+ *   stream is left unwritten); 1 <= n <= ring (a longer span is refused with TFD_ERR_INVALID);
+ *   k_ring, v_ring device bf16 [streams][ring][heads][dim]; dim == 128.
+ */
+tfd_status tfd_absorb(const void* k_rows, const void* v_rows, const void* k_gamma, float eps,
+                      float rope_base, const int32_t* p0, int n, void* k_ring, void* v_ring,
+                      int ring, int streams, int heads, int dim, int32_t* dev_status,
+                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

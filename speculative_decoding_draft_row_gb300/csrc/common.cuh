@@ -124,9 +124,11 @@ inline int sm_count() {
 // Internal launchers shared across translation units.
 namespace tfd_internal {
 // Top-k over fp32 logits by a threshold filter, one thread-block cluster per row (topk.cu). The
-// workspace is tfd_topk_workspace() bytes.
+// workspace is tfd_topk_workspace() bytes. pre_max, when not null, already holds the value key of
+// the maximum of every 16-logit sub-group of each row, [rows][ceil(n / 16)], so the logits are
+// read only where a sub-group can reach the threshold.
 tfd_status topk_launch(const float* logits, int rows, int64_t n, int64_t ld, int k,
-                       const int32_t* id_map, float* vals, int32_t* ids, int64_t ld_out, void* ws,
-                       size_t ws_bytes, cudaStream_t stream);
+                       const int32_t* id_map, float* vals, int32_t* ids, int64_t ld_out,
+                       const uint32_t* pre_max, void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t topk_workspace(int rows, int64_t n, int k);
 }  // namespace tfd_internal

@@ -18,6 +18,8 @@
 // and activations so that each thread's 16 contiguous bytes are one MMA operand chunk.
 // Per group, the four k-slice partials are summed in a fixed order in shared memory, so every
 // output's arithmetic is independent of its index and of the part count.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace {
@@ -43,9 +45,14 @@ namespace {
 #ifndef TFD_GEMV_MINB_NT1
 #define TFD_GEMV_MINB_NT1 1
 #endif
-template <int WF, int NT>
+// fp32 activations take three planes of MMA operands; their two-n-tile form keeps a shallower ring
+#ifndef TFD_GEMV_DEPTH_X32_NT2
+#define TFD_GEMV_DEPTH_X32_NT2 4
+#endif
+template <int WF, int NT, int XF = TFD_X_BF16>
 constexpr int gemv_depth() {
-  return WF == TFD_W_BF16 ? (NT == 1 ? TFD_GEMV_DEPTH_NT1 : TFD_GEMV_DEPTH_NT2)
+  return (XF == TFD_X_F32 && NT == 2) ? TFD_GEMV_DEPTH_X32_NT2
+       : WF == TFD_W_BF16 ? (NT == 1 ? TFD_GEMV_DEPTH_NT1 : TFD_GEMV_DEPTH_NT2)
        : WF == TFD_W_FP8_ROW ? (NT == 1 ? TFD_GEMV_DEPTH_FP8_NT1 : TFD_GEMV_DEPTH_FP8_NT2)
                              : (NT == 1 ? TFD_GEMV_DEPTH_FP8_NT1 : TFD_GEMV_DEPTH_BLK_NT2);
 }
@@ -54,7 +61,6 @@ using namespace tfd;
 
 constexpr int kThreads = 512;
 constexpr int kWarps = 16;
-constexpr int kGroupRows = 64;  // 4 row tiles of 16
 constexpr int kMaxParts = 1024;
 constexpr int kMaxRowsPad = 16;
 
@@ -87,6 +93,7 @@ struct GemvArgs {
   const int32_t* id_map;
   float* logits;  // fp32 logits destination for topk > 1 (may equal y), else null
   int64_t ld_logits;
+  uint32_t* submax;  // topk > 1: [rows][ceil(n / 16)] value key of each 16-row sub-group's max
   uint64_t* part_keys;  // [parts][16]
   uint32_t* counter;
   float* top_vals;
@@ -97,6 +104,7 @@ struct GemvArgs {
   int parts;
   int64_t ngroups;
   int ssl;  // steps per k slice
+  int csplit;  // blocks of a cluster splitting k (1: no cluster); parts counts clusters
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -117,6 +125,17 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// d = A B (a zero accumulator input): starts a block's partial sum without zeroing registers.
+__device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                uint32_t a2, uint32_t a3, uint32_t b0,
+                                                uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 // Four E4M3 codes -> two f16x2 words (codes 0,1 and codes 2,3). Every E4M3 value is an f16 value,
@@ -149,7 +168,7 @@ __device__ __forceinline__ float e8m0_scale(uint32_t byte) {
 template <int WF>
 struct WLoad {
   uint32_t r[2][WTraits<WF>::WORDS];  // rows g and g + 8
-  float sc[2];                        // the step's two block scales (FP8_BLOCK32)
+  uint32_t scb;                       // the step's two E8M0 scale bytes (FP8_BLOCK32): A | B << 8
 };
 
 // An fp32 value split into three parts of the MMA operand type (bf16 for bf16 weights, f16 for
@@ -171,39 +190,57 @@ __device__ __forceinline__ void split3(float v, uint16_t& h0, uint16_t& h1, uint
   }
 }
 
-template <int WF, int XF, int NT>
+// KSL = k-slices per block: 4 (16 warps = 4 row tiles x 4 k-slices, 64-row groups) or 1 (16 row
+// tiles over the whole k range, 256-row groups: for short k, where 4 slices would leave each warp
+// only a step or two per group).
+template <int WF, int XF, int NT, int KSL = 4>
 struct Layout {
   static constexpr int E = WTraits<WF>::E;
   static constexpr int H = E / 8;                    // 16-byte x chunks per (step, nt) per lane
   static constexpr int PL = XF == TFD_X_F32 ? 3 : 1; // activation planes
-  __host__ __device__ static size_t x_bytes(int ssl) { return (size_t)PL * 4 * ssl * NT * H * 32 * 16; }
-  __host__ __device__ static size_t red_bytes() { return (size_t)2 * kWarps * NT * 32 * 16; }
+  static constexpr int MT = 16 / KSL;                // row tiles per block
+  __host__ __device__ static size_t x_bytes(int ssl) {
+    return (size_t)PL * KSL * ssl * NT * H * 32 * 16;
+  }
+  __host__ __device__ static size_t red_bytes() {
+    return KSL == 1 ? 0 : (size_t)2 * kWarps * NT * 32 * 16;
+  }
   __host__ __device__ static size_t best_bytes() {
     // block best keys, join keys, per-row x max and x scale, block (max, sum) pairs, join pairs
-    return (size_t)4 * 16 * 8 + 16 * kWarps * 8 + 2 * 16 * 4 + 4 * 16 * 8 + 16 * kWarps * 8;
+    return (size_t)MT * 16 * 8 + 16 * kWarps * 8 + 2 * 16 * 4 + MT * 16 * 8 + 16 * kWarps * 8;
   }
-  __host__ __device__ static size_t smem_bytes(int ssl) { return x_bytes(ssl) + red_bytes() + best_bytes(); }
+  // group partials of a block for its cluster leader, double-buffered (4 k-slices only)
+  __host__ __device__ static size_t cpart_bytes() {
+    return KSL == 1 ? 0 : (size_t)2 * 4 * NT * 32 * 16;
+  }
+  __host__ __device__ static size_t smem_bytes(int ssl) {
+    return x_bytes(ssl) + red_bytes() + cpart_bytes() + best_bytes();
+  }
 };
 
-template <int WF, int XF, int NT, int D>
+template <int WF, int XF, int NT, int D, int KSL>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? TFD_GEMV_MINB_NT1 : 1)
 gemv_kernel(const GemvArgs a) {
-  using L = Layout<WF, XF, NT>;
+  using L = Layout<WF, XF, NT, KSL>;
+  constexpr int MT = L::MT;
+  constexpr int GR = 16 * MT;  // rows per group
   using T = WTraits<WF>;
   constexpr int E = T::E, H = L::H, PL = L::PL, EB = T::ELEM_BYTES;
   constexpr int MMAJ = E / 4;   // k16 MMAs per step per n-tile
   constexpr int STEPK = 4 * E;  // k elements per step (4 threads x E)
   extern __shared__ __align__(16) unsigned char smem[];
   const int ssl = a.ssl;
-  const int spad = 4 * ssl;
+  const int spad = KSL * ssl;
   uint4* xs = reinterpret_cast<uint4*>(smem);
   float4* red = reinterpret_cast<float4*>(smem + L::x_bytes(ssl));
-  uint64_t* sbest = reinterpret_cast<uint64_t*>(smem + L::x_bytes(ssl) + L::red_bytes());
-  uint64_t* sjoin = sbest + 64;
+  float4* cpart = reinterpret_cast<float4*>(smem + L::x_bytes(ssl) + L::red_bytes());
+  uint64_t* sbest =
+      reinterpret_cast<uint64_t*>(smem + L::x_bytes(ssl) + L::red_bytes() + L::cpart_bytes());
+  uint64_t* sjoin = sbest + MT * 16;
   uint32_t* sxmax = reinterpret_cast<uint32_t*>(sjoin + 16 * kWarps);
   float* sxscale = reinterpret_cast<float*>(sxmax + 16);
-  float2* sms = reinterpret_cast<float2*>(sxscale + 16);   // [4][16]
-  float2* sjms = sms + 64;                                  // [kWarps][16]
+  float2* sms = reinterpret_cast<float2*>(sxscale + 16);   // [MT][16]
+  float2* sjms = sms + MT * 16;                             // [kWarps][16]
   __shared__ int is_last;
   // FP8 weights run f16 MMAs: each activation row is scaled by a power of two 2^-e_r into f16 range
   // (max |x| in [2^14, 2^15)), which keeps every bf16 activation exact down to 2^-32 of the row's
@@ -211,11 +248,131 @@ gemv_kernel(const GemvArgs a) {
   constexpr bool F16 = WF != TFD_W_BF16;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-  const int mt = warp & 3, ks = warp >> 2;
+  const int mt = warp % MT, ks = warp / MT;
+  // Split k over a cluster (small vocabularies): block crank of cluster cid takes k-slices
+  // 4 crank .. 4 crank + 3 of every group of the cluster; the leader (crank 0) sums the blocks'
+  // partials in rank order and runs the epilogue.
+  namespace cg = cooperative_groups;
+  const int csplit = KSL == 1 ? 1 : a.csplit;
+  const int crank = csplit > 1 ? (int)cg::this_cluster().block_rank() : 0;
+  const int cid = blockIdx.x / csplit;
+  const int kstep0 = crank * KSL * ssl;  // first step of this block's k range
   const int64_t K = a.k, N = a.n;
   const int rows = a.rows;
 
-  if (tid < 64) sbest[tid] = 0ull;
+  // ---- weight stream ----
+  const int64_t g_begin = (int64_t)cid * a.ngroups / a.parts;
+  const int64_t g_end = (int64_t)(cid + 1) * a.ngroups / a.parts;
+  const int s_loc = ks * ssl;              // the k-slice's first step in shared memory
+  const int s_begin = kstep0 + s_loc;      // ... and in the row
+  // The loop runs a multiple of D steps per group so the register ring stays in phase; steps past
+  // the slice's own ssl are empty (no loads, zero weights).
+  const int ssl_loop = (ssl + D - 1) / D * D;
+  const unsigned char* wbase = reinterpret_cast<const unsigned char*>(a.w);
+  const int64_t row_bytes = K * EB;
+  const uint8_t* blk_scales = reinterpret_cast<const uint8_t*>(a.scales);
+  const float* row_scales = reinterpret_cast<const float*>(a.scales);
+  const int64_t kblocks = K >> 5;
+  const bool sc16 = (kblocks & 1) == 0;  // a step's two scale bytes are 2-byte aligned
+
+  // The thread's first element in a step: its 16 contiguous elements, or (block-32 form) its 8
+  // elements of the step's first 32-wide block, the other 8 being 32 further on.
+  const int toff = WF == TFD_W_FP8_BLOCK32 ? 8 * t : t * E;
+  auto steps_below = [&](int64_t lim) -> int {  // steps s < ssl with (s_begin + s) * STEPK < lim
+    int64_t v = lim > 0 ? (lim + STEPK - 1) / STEPK - s_begin : 0;
+    return (int)(v < 0 ? 0 : (v > ssl ? ssl : v));
+  };
+  const int nvalid = steps_below(K - toff);
+  const int nvalid_b = WF == TFD_W_FP8_BLOCK32 ? steps_below(K - 32 - toff) : nvalid;
+
+  // Load state: group, step, row pointer and row validity; addresses advance by a constant.
+  int64_t ld_g = g_begin;
+  int ld_s = 0;
+  const unsigned char* lp = nullptr;
+  const uint8_t* sp = nullptr;
+  bool rv0 = false, rv1 = false, rvb = false;
+  auto set_group = [&]() {
+    const int64_t row = ld_g * GR + mt * 16 + g;
+    const bool in = ld_g < g_end;
+    rv0 = in && row < N;
+    rv1 = in && row + 8 < N;
+    lp = wbase + row * row_bytes + ((int64_t)s_begin * STEPK + toff) * EB;
+    if (WF == TFD_W_FP8_BLOCK32) {
+      const int64_t rblk = (ld_g * GR + mt * 16) >> 5;
+      rvb = in && rblk * 32 < N;
+      sp = blk_scales + rblk * kblocks + 2 * (int64_t)s_begin;
+    }
+  };
+  set_group();
+  auto issue = [&](WLoad<WF>& b) {
+    // the usual step: both rows and (block-32 form) both blocks in range, no zero fill
+    const bool full = rv1 && ld_s < (WF == TFD_W_FP8_BLOCK32 ? nvalid_b : nvalid) &&
+                      (WF != TFD_W_FP8_BLOCK32 || sc16);
+    if (full) {
+      if (WF == TFD_W_FP8_BLOCK32) {
+        uint2 v = ldg_stream8(lp);
+        b.r[0][0] = v.x; b.r[0][1] = v.y;
+        v = ldg_stream8(lp + 32);
+        b.r[0][2] = v.x; b.r[0][3] = v.y;
+        v = ldg_stream8(lp + 8 * row_bytes);
+        b.r[1][0] = v.x; b.r[1][1] = v.y;
+        v = ldg_stream8(lp + 8 * row_bytes + 32);
+        b.r[1][2] = v.x; b.r[1][3] = v.y;
+        b.scb = __ldg(reinterpret_cast<const uint16_t*>(sp));
+      } else {
+        uint4 v = ldg_stream16(lp);
+        b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
+        v = ldg_stream16(lp + 8 * row_bytes);
+        b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
+      }
+      lp += STEPK * EB;
+      sp += 2;
+      if (++ld_s == ssl_loop) { ld_s = 0; ++ld_g; set_group(); }
+      return;
+    }
+#pragma unroll
+    for (int i = 0; i < T::WORDS; ++i) { b.r[0][i] = 0u; b.r[1][i] = 0u; }
+    b.scb = 0u;
+    if (ld_s < nvalid) {
+      if (WF == TFD_W_FP8_BLOCK32) {
+        const bool second = ld_s < nvalid_b;
+        if (rv0) {
+          uint2 v = ldg_stream8(lp);
+          b.r[0][0] = v.x; b.r[0][1] = v.y;
+          if (second) { v = ldg_stream8(lp + 32); b.r[0][2] = v.x; b.r[0][3] = v.y; }
+        }
+        if (rv1) {
+          uint2 v = ldg_stream8(lp + 8 * row_bytes);
+          b.r[1][0] = v.x; b.r[1][1] = v.y;
+          if (second) { v = ldg_stream8(lp + 8 * row_bytes + 32); b.r[1][2] = v.x; b.r[1][3] = v.y; }
+        }
+        if (rvb) {
+          if (sc16) b.scb = __ldg(reinterpret_cast<const uint16_t*>(sp));
+          else b.scb = (uint32_t)__ldg(sp) | ((uint32_t)__ldg(sp + 1) << 8);
+          if (!second) b.scb &= 0xFFu;
+        }
+      } else {
+        if (rv0) {
+          uint4 v = ldg_stream16(lp);
+          b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
+        }
+        if (rv1) {
+          uint4 v = ldg_stream16(lp + 8 * row_bytes);
+          b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
+        }
+      }
+    }
+    lp += STEPK * EB;
+    sp += 2;
+    if (++ld_s == ssl_loop) { ld_s = 0; ++ld_g; set_group(); }
+  };
+
+  // The first D steps of weights are in flight while the activations are staged.
+  WLoad<WF> buf[D];
+#pragma unroll
+  for (int i = 0; i < D; ++i) issue(buf[i]);
+
+  for (int i = tid; i < MT * 16; i += kThreads) sbest[i] = 0ull;
   if (tid < 16) sxmax[tid] = 0u;
   __syncthreads();
   if (F16) {
@@ -260,22 +417,23 @@ gemv_kernel(const GemvArgs a) {
     for (int idx = tid; idx < total; idx += kThreads) {
       const int r = idx / chunks_per_row;
       const int c = idx - r * chunks_per_row;
-      const int k0 = c * 8;
+      const int k0 = c * 8;  // within the block's k range
       const int s = k0 / STEPK;
       const int rem = k0 - s * STEPK;
+      const int64_t kg = (int64_t)kstep0 * STEPK + k0;  // in the whole row
       // A thread's 16-element chunk is contiguous, except in the block-32 form, where it is 8 elements
       // of each 32-wide scale block of the step (so every MMA stays inside one block).
       const int tt = WF == TFD_W_FP8_BLOCK32 ? (rem & 31) >> 3 : rem / E;
       const int hf = WF == TFD_W_FP8_BLOCK32 ? rem >> 5 : (rem - tt * E) >> 3;
       const int ln = (r & 7) * 4 + tt;
       const int nt = r >> 3;
-      const bool ok = r < rows && k0 < K;
+      const bool ok = r < rows && kg < K;
       const float inv = F16 ? __uint_as_float(sxmax[r]) : 1.0f;
       if (XF == TFD_X_BF16 && !F16) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (ok)
           v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
-                                              (int64_t)r * a.ldx + k0);
+                                              (int64_t)r * a.ldx + kg);
         xs[((s * NT + nt) * H + hf) * 32 + ln] = v;
       } else {
         float f[8];
@@ -284,13 +442,13 @@ gemv_kernel(const GemvArgs a) {
         if (ok) {
           if (XF == TFD_X_BF16) {
             uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
-                                                      (int64_t)r * a.ldx + k0);
+                                                      (int64_t)r * a.ldx + kg);
             uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) { f[2 * i] = bf16_lo(u[i]); f[2 * i + 1] = bf16_hi(u[i]); }
           } else {
             const float4* p = reinterpret_cast<const float4*>(
-                reinterpret_cast<const float*>(a.x) + (int64_t)r * a.ldx + k0);
+                reinterpret_cast<const float*>(a.x) + (int64_t)r * a.ldx + kg);
             float4 u = p[0], w = p[1];
             f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
             f[4] = w.x; f[5] = w.y; f[6] = w.z; f[7] = w.w;
@@ -316,89 +474,47 @@ gemv_kernel(const GemvArgs a) {
   }
   __syncthreads();
 
-  // ---- weight stream ----
-  const int64_t g_begin = (int64_t)blockIdx.x * a.ngroups / a.parts;
-  const int64_t g_end = (int64_t)(blockIdx.x + 1) * a.ngroups / a.parts;
-  const int s_begin = ks * ssl;
-  // The loop runs a multiple of D steps per group so the register ring stays in phase; steps past
-  // the slice's own ssl are empty (no loads, zero weights).
-  const int ssl_loop = (ssl + D - 1) / D * D;
-  const unsigned char* wbase = reinterpret_cast<const unsigned char*>(a.w);
-  const int64_t row_bytes = K * EB;
-  const uint8_t* blk_scales = reinterpret_cast<const uint8_t*>(a.scales);
-  const float* row_scales = reinterpret_cast<const float*>(a.scales);
-  const int64_t kblocks = K >> 5;
-
-  // The thread's first element in a step: its 16 contiguous elements, or (block-32 form) its 8
-  // elements of the step's first 32-wide block, the other 8 being 32 further on.
-  const int toff = WF == TFD_W_FP8_BLOCK32 ? 8 * t : t * E;
-  auto steps_below = [&](int64_t lim) -> int {  // steps s < ssl with (s_begin + s) * STEPK < lim
-    int64_t v = lim > 0 ? (lim + STEPK - 1) / STEPK - s_begin : 0;
-    return (int)(v < 0 ? 0 : (v > ssl ? ssl : v));
-  };
-  const int nvalid = steps_below(K - toff);
-  const int nvalid_b = WF == TFD_W_FP8_BLOCK32 ? steps_below(K - 32 - toff) : nvalid;
-
-  // Load state: group, step, row pointer and row validity; addresses advance by a constant.
-  int64_t ld_g = g_begin;
-  int ld_s = 0;
-  const unsigned char* lp = nullptr;
-  const uint8_t* sp = nullptr;
-  bool rv0 = false, rv1 = false, rvb = false;
-  auto set_group = [&]() {
-    const int64_t row = ld_g * kGroupRows + mt * 16 + g;
-    const bool in = ld_g < g_end;
-    rv0 = in && row < N;
-    rv1 = in && row + 8 < N;
-    lp = wbase + row * row_bytes + ((int64_t)s_begin * STEPK + toff) * EB;
-    if (WF == TFD_W_FP8_BLOCK32) {
-      const int64_t rblk = (ld_g * kGroupRows + mt * 16) >> 5;
-      rvb = in && rblk * 32 < N;
-      sp = blk_scales + rblk * kblocks + 2 * (int64_t)s_begin;
-    }
-  };
-  set_group();
-  auto issue = [&](WLoad<WF>& b) {
-#pragma unroll
-    for (int i = 0; i < T::WORDS; ++i) { b.r[0][i] = 0u; b.r[1][i] = 0u; }
-    b.sc[0] = 0.0f;
-    b.sc[1] = 0.0f;
-    if (ld_s < nvalid) {
-      if (WF == TFD_W_FP8_BLOCK32) {
-        const bool second = ld_s < nvalid_b;
-        if (rv0) {
-          uint2 v = ldg_stream8(lp);
-          b.r[0][0] = v.x; b.r[0][1] = v.y;
-          if (second) { v = ldg_stream8(lp + 32); b.r[0][2] = v.x; b.r[0][3] = v.y; }
-        }
-        if (rv1) {
-          uint2 v = ldg_stream8(lp + 8 * row_bytes);
-          b.r[1][0] = v.x; b.r[1][1] = v.y;
-          if (second) { v = ldg_stream8(lp + 8 * row_bytes + 32); b.r[1][2] = v.x; b.r[1][3] = v.y; }
-        }
-        if (rvb) {
-          b.sc[0] = e8m0_scale(__ldg(sp));
-          if (second) b.sc[1] = e8m0_scale(__ldg(sp + 1));
-        }
-      } else {
-        if (rv0) {
-          uint4 v = ldg_stream16(lp);
-          b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
-        }
-        if (rv1) {
-          uint4 v = ldg_stream16(lp + 8 * row_bytes);
-          b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
-        }
-      }
-    }
-    lp += STEPK * EB;
-    sp += 2;
-    if (++ld_s == ssl_loop) { ld_s = 0; ++ld_g; set_group(); }
-  };
 
   // One step: MMA j of the step takes elements [4j, 4j + 4) of each thread's chunk. All activation
   // fragments of the step are read first; each weight fragment is widened just before its MMAs.
+  // Block-32 form: the step is two 32-wide blocks (MMAs 0-1 and 2-3), each summed on its own and
+  // added to the accumulator times its scale; its activation fragments are read per block, which
+  // keeps fewer registers live.
   auto compute = [&](const WLoad<WF>& b, int sg, float (&acc)[NT][4]) {
+    if constexpr (WF == TFD_W_FP8_BLOCK32) {
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t xq[NT][PL][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int pl = 0; pl < PL; ++pl) {
+            const uint4 v = xs[(((pl * spad + sg) * NT + nt) * H + hb) * 32 + lane];
+            xq[nt][pl][0] = v.x; xq[nt][pl][1] = v.y; xq[nt][pl][2] = v.z; xq[nt][pl][3] = v.w;
+          }
+        float c[NT][4];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          uint32_t A0, A1, A2, A3;
+          e4m3x4_to_f16x2(b.r[0][2 * hb + jj], A0, A2);
+          e4m3x4_to_f16x2(b.r[1][2 * hb + jj], A1, A3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int pl = 0; pl < PL; ++pl) {
+              if (jj == 0 && pl == 0)  // the block's first MMA starts its partial sum
+                mma_f16_16816_z(c[nt], A0, A1, A2, A3, xq[nt][pl][0], xq[nt][pl][1]);
+              else
+                mma_f16_16816(c[nt], A0, A1, A2, A3, xq[nt][pl][2 * jj], xq[nt][pl][2 * jj + 1]);
+            }
+        }
+        const float sc = e8m0_scale((b.scb >> (8 * hb)) & 0xFFu);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[nt][i] = fmaf(sc, c[nt][i], acc[nt][i]);
+      }
+    } else {
     uint32_t xw[NT][PL][4 * H];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -414,7 +530,7 @@ gemv_kernel(const GemvArgs a) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) c[nt][i] = (WF == TFD_W_FP8_BLOCK32) ? 0.0f : acc[nt][i];
+      for (int i = 0; i < 4; ++i) c[nt][i] = acc[nt][i];
 #pragma unroll
     for (int j = 0; j < MMAJ; ++j) {
       uint32_t A0, A1, A2, A3;
@@ -431,32 +547,28 @@ gemv_kernel(const GemvArgs a) {
           if (F16) mma_f16_16816(c[nt], A0, A1, A2, A3, xw[nt][pl][2 * j], xw[nt][pl][2 * j + 1]);
           else mma_bf16_16816(c[nt], A0, A1, A2, A3, xw[nt][pl][2 * j], xw[nt][pl][2 * j + 1]);
         }
-      if (WF == TFD_W_FP8_BLOCK32 && (j & 1)) {
-        // MMAs 0-1 cover the step's first 32-wide block, 2-3 its second: scale each block's sum
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            acc[nt][i] = fmaf(b.sc[j >> 1], c[nt][i], acc[nt][i]);
-            c[nt][i] = 0.0f;
-          }
-      }
     }
-    if (WF != TFD_W_FP8_BLOCK32) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[nt][i] = c[nt][i];
+      for (int i = 0; i < 4; ++i) acc[nt][i] = c[nt][i];
     }
   };
 
   // Epilogue of one output value: scale, store, rank.
-  uint64_t best[2] = {0ull, 0ull};
+  // slot = 2 * n-tile + (act & 1); with 4 k-slices a reducer warp handles one n-tile
+  constexpr int BS = KSL == 1 ? 2 * NT : 2;
+  uint64_t best[BS];
+#pragma unroll
+  for (int i = 0; i < BS; ++i) best[i] = 0ull;
   // online softmax state (max, sum of exp(v - max)) of this thread's outputs, for the confidence
-  float2 ms[2] = {make_float2(-INFINITY, 0.0f), make_float2(-INFINITY, 0.0f)};
+  float2 ms[BS];
+#pragma unroll
+  for (int i = 0; i < BS; ++i) ms[i] = make_float2(-INFINITY, 0.0f);
   const bool want_conf = a.topk == 1 && a.top1_conf != nullptr;
-  auto epi = [&](int64_t row, int act, float v, int slot) {
-    if (row >= N || act >= rows) return;
+  // Returns the stored value (NaN outside the output).
+  auto epi = [&](int64_t row, int act, float v, int slot) -> float {
+    if (row >= N || act >= rows) return __uint_as_float(0x7FC00000u);
     if (F16) v *= sxscale[act];
     if (WF == TFD_W_FP8_ROW) v *= __ldg(row_scales + row);
     const int64_t yi = (int64_t)act * a.ldy + row;
@@ -482,11 +594,36 @@ gemv_kernel(const GemvArgs a) {
     } else if (a.logits != nullptr && a.logits != a.y) {
       a.logits[(int64_t)act * a.ld_logits + row] = v;
     }
+    return v;
   };
 
-  WLoad<WF> buf[D];
+  // Epilogue of one finished MMA tile (rows g, g + 8 of tile `tile` of group gi; activations act0,
+  // act0 + 1), and the tile's sub-group maximum for a later top-k.
+  auto finish_tile = [&](int64_t gi, int tile, int act0, float4 v, int slot0) {
+    const int64_t row_lo = gi * GR + tile * 16 + g;
+    const float o0 = epi(row_lo, act0, v.x, slot0);
+    const float o1 = epi(row_lo, act0 + 1, v.y, slot0 + 1);
+    const float o2 = epi(row_lo + 8, act0, v.z, slot0);
+    const float o3 = epi(row_lo + 8, act0 + 1, v.w, slot0 + 1);
+    if (a.submax != nullptr) {
+      // the 16 rows of this MMA tile are one sub-group: rows g and g + 8 of the eight lanes that
+      // share t
+      uint32_t m0 = max(value_key(o0), value_key(o2));
+      uint32_t m1 = max(value_key(o1), value_key(o3));
 #pragma unroll
-  for (int i = 0; i < D; ++i) issue(buf[i]);
+      for (int o = 4; o <= 16; o <<= 1) {
+        m0 = max(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+        m1 = max(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+      }
+      const int64_t sg = gi * MT + tile;
+      const int64_t S = (N + 15) / 16;
+      if (g == 0 && sg < S) {
+        if (act0 < rows) a.submax[(int64_t)act0 * S + sg] = m0;
+        if (act0 + 1 < rows) a.submax[(int64_t)(act0 + 1) * S + sg] = m1;
+      }
+    }
+  };
+
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -499,10 +636,19 @@ gemv_kernel(const GemvArgs a) {
 #pragma unroll
       for (int st = 0; st < D; ++st) {
         // an empty step (past ssl) reads any valid activation slot: its weights are zero
-        compute(buf[st], s_begin + (s0 + st < ssl ? s0 + st : 0), acc);
+        compute(buf[st], s_loc + (s0 + st < ssl ? s0 + st : 0), acc);
         issue(buf[st]);
       }
     }
+    if constexpr (KSL == 1) {  // the warp holds whole dot products: epilogue straight away
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        finish_tile(gi, mt, nt * 8 + 2 * t, make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]),
+                    2 * nt);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+      }
+    } else {
     // k-slice partials -> shared memory; fixed-order sum; epilogue.
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -520,43 +666,62 @@ gemv_kernel(const GemvArgs a) {
         float4 u = red[((rb * kWarps + ksi * 4 + mr) * NT + nr) * 32 + lane];
         v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
       }
-      const int64_t row_lo = gi * kGroupRows + mr * 16 + g;
-      const int act0 = nr * 8 + 2 * t;
-      epi(row_lo, act0, v.x, 0);
-      epi(row_lo, act0 + 1, v.y, 1);
-      epi(row_lo + 8, act0, v.z, 0);
-      epi(row_lo + 8, act0 + 1, v.w, 1);
+      if (csplit == 1) finish_tile(gi, mr, nr * 8 + 2 * t, v, 0);
+      else cpart[(rb * 4 * NT + warp) * 32 + lane] = v;
+    }
+    if (csplit > 1) {
+      cg::this_cluster().sync();  // every block's partial of group gi is in its shared memory
+      if (crank == 0 && warp < 4 * NT) {
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int q = 0; q < csplit; ++q) {  // blocks in rank order
+          const float4 u = cg::this_cluster().map_shared_rank(cpart, q)[(rb * 4 * NT + warp) * 32 + lane];
+          v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+        }
+        finish_tile(gi, mr, nr * 8 + 2 * t, v, 0);
+      }
+      // buffer rb is written again two groups on, after the next barrier: the leader has read it
+    }
     }
     rb ^= 1;
+  }
+  if (csplit > 1) {
+    cg::this_cluster().sync();  // the leader has read every block's last partial
+    if (crank != 0) return;
   }
 
   if (a.topk != 1) return;
   // ---- top-1: block best per row, then the last block to finish joins the parts ----
-  if (warp < 4 * NT) {
+  if (KSL == 1 || warp < 4 * NT) {
+    // the tile this warp finished, and its n-tiles: (mr, nr) with 4 k-slices, (mt, all) with one
+    const int tile = KSL == 1 ? mt : mr;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      uint64_t key = best[c];
+    for (int sl = 0; sl < BS; ++sl) {
+      const int nt = KSL == 1 ? sl >> 1 : nr;
+      const int c = sl & 1;
+      uint64_t key = best[sl];
       key = umax64(key, shfl_xor_u64(key, 4));
       key = umax64(key, shfl_xor_u64(key, 8));
       key = umax64(key, shfl_xor_u64(key, 16));
-      if (g == 0) sbest[mr * 16 + nr * 8 + 2 * t + c] = key;
+      if (g == 0) sbest[tile * 16 + nt * 8 + 2 * t + c] = key;
       if (want_conf) {
-        float2 q = ms[c];
+        float2 q = ms[sl];
 #pragma unroll
         for (int o = 4; o <= 16; o <<= 1)
           q = ms_merge(q, make_float2(__shfl_xor_sync(0xffffffffu, q.x, o),
                                       __shfl_xor_sync(0xffffffffu, q.y, o)));
-        if (g == 0) sms[mr * 16 + nr * 8 + 2 * t + c] = q;
+        if (g == 0) sms[tile * 16 + nt * 8 + 2 * t + c] = q;
       }
     }
   }
   __syncthreads();
-  if (tid < kMaxRowsPad) {
-    uint64_t m = umax64(umax64(sbest[tid], sbest[16 + tid]), umax64(sbest[32 + tid], sbest[48 + tid]));
-    a.part_keys[(int64_t)blockIdx.x * kMaxRowsPad + tid] = m;
+  if (tid < kMaxRowsPad) {  // tiles merged in a fixed order
+    uint64_t m = sbest[tid];
+    for (int i = 1; i < MT; ++i) m = umax64(m, sbest[i * 16 + tid]);
+    a.part_keys[(int64_t)cid * kMaxRowsPad + tid] = m;
     if (want_conf) {
-      const float2 q = ms_merge(ms_merge(sms[tid], sms[16 + tid]), ms_merge(sms[32 + tid], sms[48 + tid]));
-      a.part_ms[(int64_t)blockIdx.x * kMaxRowsPad + tid] = q;
+      float2 q = sms[tid];
+      for (int i = 1; i < MT; ++i) q = ms_merge(q, sms[i * 16 + tid]);
+      a.part_ms[(int64_t)cid * kMaxRowsPad + tid] = q;
     }
   }
   __threadfence();
@@ -614,40 +779,87 @@ gemv_kernel(const GemvArgs a) {
 
 constexpr size_t kSmemLimit = 232448 - 1024;   // sm_100-class dynamic shared memory, minus slack
 
-template <int WF, int XF, int NT>
+template <int WF, int XF, int NT, int KSL = 4>
 size_t gemv_smem(int64_t k, int* ssl_out) {
   constexpr int E = WTraits<WF>::E;
   int64_t steps = (k + 4 * E - 1) / (4 * E);
-  int64_t ssl = (steps + 3) / 4;
+  int64_t ssl = (steps + KSL - 1) / KSL;
   if (ssl_out) *ssl_out = (int)ssl;
-  return Layout<WF, XF, NT>::smem_bytes((int)ssl);
+  return Layout<WF, XF, NT, KSL>::smem_bytes((int)ssl);
 }
 
-template <int WF, int XF, int NT>
-tfd_status gemv_launch_t(GemvArgs a, int parts_req, cudaStream_t stream) {
+template <int WF, int XF, int NT, int KSL>
+tfd_status gemv_launch_k(GemvArgs a, int parts_req, cudaStream_t stream) {
   int ssl = 0;
-  size_t smem = gemv_smem<WF, XF, NT>(a.k, &ssl);
+  size_t smem = gemv_smem<WF, XF, NT, KSL>(a.k, &ssl);
   if (smem > kSmemLimit) return TFD_ERR_UNSUPPORTED;
-  auto kern = gemv_kernel<WF, XF, NT, gemv_depth<WF, NT>()>;
+  const int64_t group_rows = 16 * (16 / KSL);
+  a.ngroups = (a.n + group_rows - 1) / group_rows;
+  auto kern = gemv_kernel<WF, XF, NT, gemv_depth<WF, NT, XF>(), KSL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit) !=
       cudaSuccess)
     return TFD_ERR_CUDA;
   int parts = parts_req;
+  int csplit = 1;
   if (parts <= 0) {
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess)
       return TFD_ERR_CUDA;
     if (occ < 1) occ = 1;
-    int64_t p = (int64_t)tfd_host::sm_count() * occ;
+    const int64_t slots = (int64_t)tfd_host::sm_count() * occ;
+    if (KSL == 4 && a.ngroups * 2 <= slots) {
+      // Too few groups for the SMs: split k over a cluster of 2, 4 or 8 blocks, keeping at least
+      // a ring's depth of steps per k-slice.
+      constexpr int E = WTraits<WF>::E;
+      constexpr int D = gemv_depth<WF, NT, XF>();
+      const int64_t steps = (a.k + 4 * E - 1) / (4 * E);
+      int64_t c = slots / a.ngroups;
+      if (c > steps / (4 * D)) c = steps / (4 * D);
+      csplit = c >= 8 ? 8 : c >= 4 ? 4 : c >= 2 ? 2 : 1;
+    }
+    int64_t p = slots / csplit;
     if (p > a.ngroups) p = a.ngroups;
     if (p > kMaxParts) p = kMaxParts;
     if (p < 1) p = 1;
     parts = (int)p;
   }
   a.parts = parts;
-  a.ssl = ssl;
-  kern<<<parts, kThreads, smem, stream>>>(a);
+  a.csplit = csplit;
+  if (csplit == 1) {
+    a.ssl = ssl;
+    kern<<<parts, kThreads, smem, stream>>>(a);
+    return tfd_host::launch_status();
+  }
+  constexpr int E = WTraits<WF>::E;
+  const int64_t steps = (a.k + 4 * E - 1) / (4 * E);
+  a.ssl = (int)((steps + 4 * csplit - 1) / (4 * csplit));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(parts * csplit));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<WF, XF, NT, KSL>::smem_bytes(a.ssl);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)csplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TFD_ERR_CUDA;
   return tfd_host::launch_status();
+}
+
+// bf16 weights with a short k (fewer than D steps per k-slice, e.g. the 256-wide second GEMV of
+// the two-stage head) and enough rows for every SM run with one k-slice and 256-row groups.
+template <int WF, int XF, int NT>
+tfd_status gemv_launch_t(GemvArgs a, int parts_req, cudaStream_t stream) {
+  if constexpr (WF == TFD_W_BF16) {
+    constexpr int D = gemv_depth<WF, NT, XF>();
+    const int64_t steps = (a.k + 4 * WTraits<WF>::E - 1) / (4 * WTraits<WF>::E);
+    if ((steps + 3) / 4 < D && (a.n + 255) / 256 >= tfd_host::sm_count())
+      return gemv_launch_k<WF, XF, NT, 1>(a, parts_req, stream);
+  }
+  return gemv_launch_k<WF, XF, NT, 4>(a, parts_req, stream);
 }
 
 template <int WF, int XF>
@@ -678,27 +890,31 @@ struct GemvWs {
   uint64_t* part_keys;
   float2* part_ms;
   float* logits;
+  uint32_t* submax;
   void* topk_ws;
   size_t topk_bytes;
 };
 
-// Workspace: [counter | part keys for top-1 | fp32 logits for top-k > 1 | top-k workspace].
+// Workspace: [counter | part keys for top-1 | fp32 logits for top-k > 1 | sub-group maxima for
+// top-k > 1 | top-k workspace].
 size_t gemv_ws_layout(int rows, int64_t n, int topk, bool logits_in_y, char* base, GemvWs* out) {
   size_t off = 256;
   // top-1: per part a key and an online-softmax pair per row
   size_t keys = topk == 1 ? tfd_host::round_up((size_t)kMaxParts * kMaxRowsPad * 8, 256) * 2 : 0;
   size_t lg = (topk > 1 && !logits_in_y) ? tfd_host::round_up((size_t)rows * n * 4, 256) : 0;
+  size_t sub = topk > 1 ? tfd_host::round_up((size_t)rows * ((n + 15) / 16) * 4, 256) : 0;
   size_t tk = topk > 1 ? tfd_internal::topk_workspace(rows, n, topk) : 0;
   if (out) {
     out->counter = reinterpret_cast<uint32_t*>(base);
     out->part_keys = keys ? reinterpret_cast<uint64_t*>(base + off) : nullptr;
     out->part_ms = keys ? reinterpret_cast<float2*>(base + off + keys / 2) : nullptr;
     out->logits = lg ? reinterpret_cast<float*>(base + off + keys) : nullptr;
-    out->topk_ws = tk ? base + off + keys + lg : nullptr;
+    out->submax = sub ? reinterpret_cast<uint32_t*>(base + off + keys + lg) : nullptr;
+    out->topk_ws = tk ? base + off + keys + lg + sub : nullptr;
     out->topk_bytes = tk;
   }
   if (topk == 0) return 0;
-  return off + keys + lg + tk;
+  return off + keys + lg + sub + tk;
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -773,9 +989,11 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   a.out_mode = out_mode; a.y = y; a.ldy = ldy; a.topk = topk; a.id_map = id_map;
   a.logits = nullptr;
   a.ld_logits = 0;
+  a.submax = nullptr;
   if (topk > 1) {
     a.logits = logits_in_y ? reinterpret_cast<float*>(y) : wl.logits;
     a.ld_logits = logits_in_y ? ldy : n;
+    a.submax = wl.submax;
   }
   a.part_keys = wl.part_keys;
   a.counter = wl.counter;
@@ -784,7 +1002,7 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   a.ldt = ldt;
   a.top1_conf = top1_conf;
   a.part_ms = wl.part_ms;
-  a.ngroups = (n + kGroupRows - 1) / kGroupRows;
+  a.ngroups = 0;  // set by the launcher for its group size
   cudaStream_t s = tfd_host::as_stream(stream);
   tfd_status st;
   if (wfmt == TFD_W_FP8_ROW) st = gemv_launch_x<TFD_W_FP8_ROW>(a, xfmt, parts, s);
@@ -792,5 +1010,5 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   else st = gemv_launch_x<TFD_W_BF16>(a, xfmt, parts, s);
   if (st != TFD_OK || topk <= 1) return st;
   return tfd_internal::topk_launch(a.logits, rows, n, a.ld_logits, topk, id_map, top_vals, top_ids,
-                                   ldt, wl.topk_ws, wl.topk_bytes, s);
+                                   ldt, wl.submax, wl.topk_ws, wl.topk_bytes, s);
 }

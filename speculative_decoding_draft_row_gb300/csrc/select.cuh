@@ -287,4 +287,46 @@ __device__ inline void block_sort_desc(uint64_t* a, int np) {
   }
 }
 
+// Sorts keys[0..c) descending for c <= 1024 (room for 1024; slots past c count as zero keys),
+// by a bitonic network over 1024 slots. Each warp holds 64 consecutive slots, two per lane, so the
+// 45 stages whose partners are at most 32 slots apart run in registers with warp shuffles; only
+// the 10 stages with partners 64 or more apart go through shared memory and block barriers.
+// Called by all kSelectThreads threads of the block; returns after a barrier.
+__device__ inline void block_sort_desc_1024(uint64_t* keys, int c) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i0 = 64 * warp + 2 * lane, i1 = i0 + 1;  // this thread's two slots
+  __syncthreads();
+  uint64_t a0 = i0 < c ? keys[i0] : 0ull;
+  uint64_t a1 = i1 < c ? keys[i1] : 0ull;
+  for (int size = 2; size <= 1024; size <<= 1) {
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      uint64_t y0, y1;
+      if (j >= 64) {  // partner in another warp
+        __syncthreads();
+        keys[i0] = a0;
+        keys[i1] = a1;
+        __syncthreads();
+        y0 = keys[i0 ^ j];
+        y1 = keys[i1 ^ j];
+      } else if (j >= 2) {  // partner lane ^ (j / 2), same register
+        y0 = shfl_xor_u64(a0, j >> 1);
+        y1 = shfl_xor_u64(a1, j >> 1);
+      } else {  // partners in the same lane
+        y0 = a1;
+        y1 = a0;
+      }
+      // keep the larger where the slot's block of `size` runs descending and it is the lower
+      // slot of the pair, or where its block runs ascending and it is the upper one
+      const bool km0 = ((i0 & size) == 0) == ((i0 & j) == 0);
+      const bool km1 = ((i1 & size) == 0) == ((i1 & j) == 0);
+      a0 = km0 ? umax64(a0, y0) : (a0 < y0 ? a0 : y0);
+      a1 = km1 ? umax64(a1, y1) : (a1 < y1 ? a1 : y1);
+    }
+  }
+  __syncthreads();
+  keys[i0] = a0;
+  keys[i1] = a1;
+  __syncthreads();
+}
+
 }  // namespace tfd

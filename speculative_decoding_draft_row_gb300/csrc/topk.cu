@@ -181,7 +181,8 @@ template <bool VEC>
 __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
 topk_cluster_kernel(const float* __restrict__ logits, int64_t n, int64_t ld, int k,
                     const int32_t* __restrict__ id_map, float* __restrict__ vals,
-                    int32_t* __restrict__ ids, int64_t ld_out, uint32_t* __restrict__ gmaxima,
+                    int32_t* __restrict__ ids, int64_t ld_out,
+                    const uint32_t* __restrict__ pre_max, uint32_t* __restrict__ gmaxima,
                     int64_t chunk) {
   extern __shared__ __align__(16) unsigned char tk_smem[];
   ClusterSmem& sm = *reinterpret_cast<ClusterSmem*>(tk_smem);
@@ -194,15 +195,30 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t n, int64_t ld, int
   const int64_t hi = lo + chunk < n ? lo + chunk : n;
   const int nsub = (int)((hi - lo + kSub - 1) / kSub);
   const int64_t sub_per_block = chunk / kSub;
-  uint32_t* maxima = sub_per_block <= kSubCap
-                         ? sm.maxima
-                         : gmaxima + ((int64_t)r * kCl + rank) * sub_per_block;
+  const int64_t S = (n + kSub - 1) / kSub;
+  uint32_t* wmax = sub_per_block <= kSubCap
+                       ? sm.maxima
+                       : gmaxima + ((int64_t)r * kCl + rank) * sub_per_block;
+  const uint32_t* maxima = wmax;
   if (tid == 0) sm.cand_count = 0u;
 
-  // ---- pass 1: the part's sub-group maxima (the only full read of the logits) ----
   uint32_t lmax = 0u;
+  if (pre_max != nullptr) {  // maxima given (written by the producer of the logits)
+    const uint32_t* src = pre_max + (int64_t)r * S + (int64_t)rank * sub_per_block;
+    if (sub_per_block <= kSubCap) {
+      for (int i = tid; i < nsub; i += kThreads) {
+        const uint32_t m = __ldcg(src + i);
+        wmax[i] = m;
+        lmax = max(lmax, m);
+      }
+    } else {
+      for (int i = tid; i < nsub; i += kThreads) lmax = max(lmax, __ldcg(src + i));
+      maxima = src;
+    }
+  }
+  // ---- pass 1: the part's sub-group maxima (the only full read of the logits) ----
   constexpr int kStep = 4 * kThreads * kUnroll;
-  for (int64_t b0 = lo; b0 < hi; b0 += kStep) {  // block-uniform bounds
+  for (int64_t b0 = pre_max ? hi : lo; b0 < hi; b0 += kStep) {  // block-uniform bounds
     float4 v[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
@@ -211,7 +227,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t n, int64_t ld, int
     for (int u = 0; u < kUnroll; ++u) {
       const uint32_t m = sub_max4(v[u]);
       const int64_t sg = (b0 - lo + 4 * (int64_t)(u * kThreads + tid)) / kSub;
-      if ((tid & 3) == 0 && sg < nsub) maxima[sg] = m;
+      if ((tid & 3) == 0 && sg < nsub) wmax[sg] = m;
       lmax = max(lmax, m);
     }
   }
@@ -222,7 +238,6 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t n, int64_t ld, int
   // ---- the threshold T <= m_k ----
   uint32_t K = 0u;
   for (int q = 0; q < kCl; ++q) K = max(K, *cluster.map_shared_rank(&sm.bmax, q));
-  const int64_t S = (n + kSub - 1) / kSub;
   const uint32_t T = S >= k ? cluster_threshold(maxima, nsub, K, k, sm) : 0u;
 
   // ---- pass 2: the logits >= T of the sub-groups whose maximum reaches T ----
@@ -277,6 +292,9 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t n, int64_t ld, int
     if (cn <= kRankMax) {
       rank_count_select(sm.cand, cn, k, sm.sel.out);
       top = sm.sel.out;
+    } else if (cn <= 1024) {
+      block_sort_desc_1024(sm.cand, cn);
+      top = sm.cand;
     } else {
       int np = 1;
       while (np < cn) np <<= 1;
@@ -316,8 +334,8 @@ size_t topk_workspace(int rows, int64_t n, int k) {
 }
 
 tfd_status topk_launch(const float* logits, int rows, int64_t n, int64_t ld, int k,
-                       const int32_t* id_map, float* vals, int32_t* ids, int64_t ld_out, void* ws,
-                       size_t ws_bytes, cudaStream_t stream) {
+                       const int32_t* id_map, float* vals, int32_t* ids, int64_t ld_out,
+                       const uint32_t* pre_max, void* ws, size_t ws_bytes, cudaStream_t stream) {
   const size_t need = topk_workspace(rows, n, k);
   if (need == 0) return TFD_ERR_INVALID;
   if (ws == nullptr || ws_bytes < need) return TFD_ERR_WORKSPACE;
@@ -328,7 +346,7 @@ tfd_status topk_launch(const float* logits, int rows, int64_t n, int64_t ld, int
       cudaSuccess)
     return TFD_ERR_CUDA;
   dim3 grid(kCl, (unsigned)rows);
-  kern<<<grid, kThreads, smem, stream>>>(logits, n, ld, k, id_map, vals, ids, ld_out,
+  kern<<<grid, kThreads, smem, stream>>>(logits, n, ld, k, id_map, vals, ids, ld_out, pre_max,
                                          reinterpret_cast<uint32_t*>(ws), part_len(n));
   return tfd_host::launch_status();
 }
@@ -349,6 +367,7 @@ extern "C" tfd_status tfd_topk(const float* logits, int rows, int64_t n, int64_t
   if (!aligned(logits, 4) || !aligned(vals, 4) || !aligned(ids, 4)) return TFD_ERR_INVALID;
   if (id_map && !aligned(id_map, 4)) return TFD_ERR_INVALID;
   if (ws && !aligned(ws, 16)) return TFD_ERR_INVALID;
-  return tfd_internal::topk_launch(logits, rows, n, ld, k, id_map, vals, ids, k, ws, ws_bytes,
+  return tfd_internal::topk_launch(logits, rows, n, ld, k, id_map, vals, ids, k, nullptr, ws,
+                                   ws_bytes,
                                    tfd_host::as_stream(stream));
 }

@@ -39,6 +39,10 @@ SIGNATURES = {
     "tfd_window_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _f32, _f32, _vp, _vp, _vp, _i32, _i32,
                                _i32, _i32, _i32, _vp, _vp, _vp]),
     "tfd_accept": (_i32, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "tfd_rmsnorm": (_i32, [_vp, _i64, _vp, _f32, _i32, _i64, _vp, _i64, _vp]),
+    "tfd_swiglu": (_i32, [_vp, _vp, _i64, _i32, _i64, _vp, _i64, _vp]),
+    "tfd_absorb": (_i32, [_vp, _vp, _vp, _f32, _f32, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
+                          _vp, _vp]),
 }
 
 _lib = None
@@ -260,3 +264,42 @@ def tfd_accept(drafts, n_asked, draws, n_kept=None, asked_hist=None, kept_hist=N
                               _p(asked_hist), _p(kept_hist), _p(dev_status), _stream(stream))
     _check("tfd_accept", st)
     return n_kept
+
+
+def tfd_rmsnorm(x, gamma=None, eps=1e-6, out=None, stream=None):
+    """RMSNorm of the rows of x [rows][hidden] (bf16). out may be x (in place). Returns out."""
+    _dev(x, gamma, out)
+    rows, hidden = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    st = library().tfd_rmsnorm(_p(x), x.stride(0), _p(gamma), float(eps), rows, hidden, _p(out),
+                               out.stride(0), _stream(stream))
+    _check("tfd_rmsnorm", st)
+    return out
+
+
+def tfd_swiglu(g, u, out=None, stream=None):
+    """bf16(bf16(SiLU(g)) * u) of two [rows][cols] bf16 tensors with the same row stride."""
+    _dev(g, u, out)
+    rows, cols = g.shape
+    if u.shape != g.shape or u.stride(0) != g.stride(0):
+        raise ValueError("g and u must have the same shape and row stride")
+    if out is None:
+        out = torch.empty_like(g)
+    st = library().tfd_swiglu(_p(g), _p(u), g.stride(0), rows, cols, _p(out), out.stride(0),
+                              _stream(stream))
+    _check("tfd_swiglu", st)
+    return out
+
+
+def tfd_absorb(k_rows, v_rows, p0, k_ring, v_ring, k_gamma=None, eps=1e-6, rope_base=10000.0,
+               dev_status=None, stream=None):
+    """Write n rows per stream (k_rows, v_rows [streams][n][heads][dim]) into the rings at positions
+    p0[s] .. p0[s] + n - 1. Refuses n > ring."""
+    _dev(k_rows, v_rows, p0, k_ring, v_ring, k_gamma)
+    streams, n, heads, dim = k_rows.shape
+    ring = k_ring.shape[1]
+    st = library().tfd_absorb(_p(k_rows), _p(v_rows), _p(k_gamma), float(eps), float(rope_base),
+                              _p(p0), n, _p(k_ring), _p(v_ring), ring, streams, heads, dim,
+                              _p(dev_status), _stream(stream))
+    _check("tfd_absorb", st)

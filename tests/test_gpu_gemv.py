@@ -49,6 +49,9 @@ SHAPES = [  # (n, k, rows, wfmt, xf32)
     (63, 16, 9, tfd.W_BF16, False),
     (4177, 4096, 16, tfd.W_BF16, False),
     (2048, 256, 16, tfd.W_BF16, True),        # fp32 activations (low-rank second GEMV)
+    (65553, 256, 16, tfd.W_BF16, True),       # short k, many rows: one k-slice, 256-row groups
+    (65536, 272, 3, tfd.W_BF16, False),
+    (40000, 64, 9, tfd.W_BF16, False),
     (1000, 272, 5, tfd.W_FP8_ROW, False),
     (4096, 4096, 4, tfd.W_FP8_ROW, False),    # wo
     (4096, 11008, 4, tfd.W_FP8_ROW, False),   # w2
@@ -113,6 +116,39 @@ def test_fused_topk_matches_own_logits_and_oracle(wfmt):
         assert np.array_equal(ti2.cpu().numpy(), oi) and same_bits(np32(tv2), ov)
         assert_sorted_keys(np32(tv), ti.cpu().numpy())
         assert_topk_valid(np32(tv), ti.cpu().numpy(), acc, S, k, what=f"top-{k}")
+
+
+def test_fused_topk_with_one_k_slice():
+    """The short-k, many-row form (one k-slice per block, 256-row groups) with a fused top-64."""
+    need_gpu()
+    case = make_case(65553, 256, 16, tfd.W_BF16, xf32=True, tid=340, tie_frac=0.01)
+    acc, S = oracle_acc_S(case, tfd.W_BF16)
+    y, tv, ti = tfd.tfd_head_gemv(case["w"], tfd.W_BF16, None, case["x"], tfd.OUT_F32, topk=64)
+    _, tv1, ti1 = tfd.tfd_head_gemv(case["w"], tfd.W_BF16, None, case["x"], tfd.OUT_F32, topk=1)
+    torch.cuda.synchronize()
+    assert_fp32_close(np32(y), acc, S, "logits")
+    ov, oi = oracle_topk(np32(y), 64)
+    assert np.array_equal(ti.cpu().numpy(), oi) and same_bits(np32(tv), ov)
+    assert np.array_equal(ti1.cpu().numpy()[:, 0], oi[:, 0])
+    assert same_bits(np32(tv1)[:, 0], ov[:, 0])
+
+
+@pytest.mark.parametrize("out_mode,rows,n", [(tfd.OUT_BF16, 16, 8192), (tfd.OUT_ADD_BF16, 5, 8000),
+                                             (tfd.OUT_NONE, 9, 8016)])
+def test_fused_topk_ranks_the_fp32_logits_in_every_output_mode(out_mode, rows, n):
+    """The fused top-k ranks the fp32 logits, whatever the stored output; a vocabulary that ends
+    inside a 64-row group and a 16-row sub-group included."""
+    need_gpu()
+    case = make_case(n, 1024, rows, tfd.W_BF16, tid=330, tie_frac=0.01)
+    y32, tv, ti = tfd.tfd_head_gemv(case["w"], tfd.W_BF16, None, case["x"], tfd.OUT_F32, topk=100)
+    y = None
+    if out_mode == tfd.OUT_ADD_BF16:
+        y = torch.zeros((rows, n), dtype=torch.bfloat16, device="cuda")
+    _, tv2, ti2 = tfd.tfd_head_gemv(case["w"], tfd.W_BF16, None, case["x"], out_mode, y=y, topk=100)
+    torch.cuda.synchronize()
+    ov, oi = oracle_topk(np32(y32), 100)
+    assert np.array_equal(ti.cpu().numpy(), oi) and same_bits(np32(tv), ov)
+    assert torch.equal(ti2, ti) and same_bits(np32(tv2), np32(tv))
 
 
 @pytest.mark.parametrize("wfmt,rows", [(tfd.W_BF16, 1), (tfd.W_BF16, 16), (tfd.W_FP8_ROW, 5)])

@@ -250,37 +250,51 @@ window_attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ 
   cluster.sync();  // keep every block's shared memory alive until block 0 has read it
 }
 
-// Absorb: one warp per (stream, row, head). The key row gets the same qk_norm, rotation and bf16
-// rounding as the window attention's current key, so a row absorbed at p equals the row the
-// attention writes at p; the value row is copied.
+// Absorb: one warp per (stream, row, 4 heads), the 4 key and value rows loaded up front. A key
+// row gets the same qk_norm, rotation and bf16 rounding as the window attention's current key, so
+// a row absorbed at p equals the row the attention writes at p; a value row is copied.
+constexpr int kAbsorbHeads = 4;
+
 __global__ void __launch_bounds__(256)
 absorb_kernel(const uint16_t* __restrict__ k_rows, const uint16_t* __restrict__ v_rows,
               const uint16_t* __restrict__ k_gamma, float eps, const RopeTurns turns,
               const int32_t* __restrict__ p0, int n, uint16_t* k_ring, uint16_t* v_ring, int ring,
               int streams, int heads, int32_t* dev_status) {
   const int lane = threadIdx.x & 31;
+  const int hgroups = (heads + kAbsorbHeads - 1) / kAbsorbHeads;
   const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (w >= (int64_t)streams * n * heads) return;  // warp-uniform
-  const int h = (int)(w % heads);
-  const int64_t si = w / heads;
+  if (w >= (int64_t)streams * n * hgroups) return;  // warp-uniform
+  const int h0 = (int)(w % hgroups) * kAbsorbHeads;
+  const int64_t si = w / hgroups;
   const int i = (int)(si % n);
   const int s = (int)(si / n);
   const int pb = p0[s];
   if (pb < 0 || pb > 2147483647 - (n - 1)) {
-    if (i == 0 && h == 0 && lane == 0) set_dev_status(dev_status, TFD_ERR_DEVICE_DATA);
+    if (i == 0 && h0 == 0 && lane == 0) set_dev_status(dev_status, TFD_ERR_DEVICE_DATA);
     return;
   }
   const int p = pb + i;
-  const int64_t src = (((int64_t)s * n + i) * heads + h) * kDim + 4 * lane;
-  const int64_t dst = (((int64_t)s * ring + p % ring) * heads + h) * kDim + 4 * lane;
-  const uint2 kraw = *reinterpret_cast<const uint2*>(k_rows + src);
-  float x[4] = {bf16_lo(kraw.x), bf16_hi(kraw.x), bf16_lo(kraw.y), bf16_hi(kraw.y)};
-  norm_rope(x, k_gamma, eps, p, turns);
-  uint2 o;
-  o.x = (uint32_t)f32_to_bf16_bits(x[0]) | ((uint32_t)f32_to_bf16_bits(x[1]) << 16);
-  o.y = (uint32_t)f32_to_bf16_bits(x[2]) | ((uint32_t)f32_to_bf16_bits(x[3]) << 16);
-  *reinterpret_cast<uint2*>(k_ring + dst) = o;
-  *reinterpret_cast<uint2*>(v_ring + dst) = *reinterpret_cast<const uint2*>(v_rows + src);
+  const int64_t src = (((int64_t)s * n + i) * heads + h0) * kDim + 4 * lane;
+  const int64_t dst = (((int64_t)s * ring + p % ring) * heads + h0) * kDim + 4 * lane;
+  uint2 kraw[kAbsorbHeads], vraw[kAbsorbHeads];
+#pragma unroll
+  for (int j = 0; j < kAbsorbHeads; ++j) {
+    if (h0 + j < heads) {
+      kraw[j] = *reinterpret_cast<const uint2*>(k_rows + src + j * kDim);
+      vraw[j] = *reinterpret_cast<const uint2*>(v_rows + src + j * kDim);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kAbsorbHeads; ++j) {
+    if (h0 + j >= heads) break;  // warp-uniform
+    float x[4] = {bf16_lo(kraw[j].x), bf16_hi(kraw[j].x), bf16_lo(kraw[j].y), bf16_hi(kraw[j].y)};
+    norm_rope(x, k_gamma, eps, p, turns);
+    uint2 o;
+    o.x = (uint32_t)f32_to_bf16_bits(x[0]) | ((uint32_t)f32_to_bf16_bits(x[1]) << 16);
+    o.y = (uint32_t)f32_to_bf16_bits(x[2]) | ((uint32_t)f32_to_bf16_bits(x[3]) << 16);
+    *reinterpret_cast<uint2*>(k_ring + dst + j * kDim) = o;
+    *reinterpret_cast<uint2*>(v_ring + dst + j * kDim) = vraw[j];
+  }
 }
 
 // The turn table of a RoPE base, computed in double on the host (kept for the last base used by
@@ -342,7 +356,7 @@ extern "C" tfd_status tfd_absorb(const void* k_rows, const void* v_rows, const v
   if (!aligned(k_rows, 16) || !aligned(v_rows, 16) || !aligned(k_ring, 16) ||
       !aligned(v_ring, 16) || !aligned(p0, 4) || (k_gamma && !aligned(k_gamma, 2)))
     return TFD_ERR_INVALID;
-  const int64_t warps = (int64_t)streams * n * heads;
+  const int64_t warps = (int64_t)streams * n * ((heads + kAbsorbHeads - 1) / kAbsorbHeads);
   if ((warps + 7) / 8 > 2147483647) return TFD_ERR_INVALID;
   absorb_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, tfd_host::as_stream(stream)>>>(
       reinterpret_cast<const uint16_t*>(k_rows), reinterpret_cast<const uint16_t*>(v_rows),

@@ -96,7 +96,7 @@ def absorb_case(S, n, H, ring, p0, tid, gamma=False):
 
 
 @pytest.mark.parametrize("S,n,H,ring,p0,gamma", [(4, 128, 32, 528, [0, 100, 512, 1000], False),
-                                                 (1, 144, 4, 144, [7], True),
+                                                 (1, 144, 6, 144, [7], True),
                                                  (2, 1, 32, 16, [3, 70000], True)])
 def test_absorb(S, n, H, ring, p0, gamma):
     need_gpu()

@@ -344,7 +344,9 @@ def run_ours(args):
 
     # ---- FP8 head, fused top-64 (reported beside the headline) ----
     fp8 = {}
-    for mode, name in ((tfd.W_FP8_BLOCK32, "e4m3_e8m0_32x32"), (tfd.W_FP8_ROW, "e4m3_row")):
+    for mode, name in ((tfd.W_FP8_BLOCK32, "e4m3_e8m0_32x32"),
+                       (tfd.W_FP8_BLOCK32_IL, "e4m3_e8m0_32x32_interleaved"),
+                       (tfd.W_FP8_ROW, "e4m3_row")):
         codes, scales = tfd.tfd_quant_fp8(wd, mode)
         ws64 = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(16, VOCAB, 64))
         out = {}
@@ -422,9 +424,11 @@ def measure_pass(wd, stream, reps=20):
     us = [inputs.normal_bf16((PASS_STREAMS, HIDDEN_FFN), 1.0, 50 + t) for t in range(PASS_STEPS)]
     resid = inputs.normal_bf16((PASS_STREAMS, HIDDEN), 1.0, 60)
     hc, hs = tfd.tfd_quant_fp8(wd, tfd.W_FP8_BLOCK32)
+    hci = tfd.tfd_fp8_block32_relayout(hc, True)
     out = {}
     for name, head, fmt, sc in (("bf16_head", wd, tfd.W_BF16, None),
-                                ("fp8_block32_head", hc, tfd.W_FP8_BLOCK32, hs)):
+                                ("fp8_block32_head", hc, tfd.W_FP8_BLOCK32, hs),
+                                ("fp8_block32_interleaved_head", hci, tfd.W_FP8_BLOCK32_IL, hs)):
         dp = DraftPass(wo_c, wo_s, w2_c, w2_s, head, fmt, sc, kr.clone().cuda(), vr.clone().cuda(),
                        PASS_WINDOW, PASS_STEPS)
         dp.load([q for q, _, _ in qkv], [k for _, k, _ in qkv], [v for _, _, v in qkv], us,
@@ -539,7 +543,8 @@ def run_fp8_case(args):
 
     torch.cuda.set_device(0)
     stream = torch.cuda.current_stream()
-    mode = tfd.W_FP8_ROW if args.fp8 == "row" else tfd.W_FP8_BLOCK32
+    mode = {"row": tfd.W_FP8_ROW, "block32": tfd.W_FP8_BLOCK32,
+            "block32il": tfd.W_FP8_BLOCK32_IL}[args.fp8]
     w, _ = inputs.head(tie_frac=0.01)
     codes, scales = tfd.tfd_quant_fp8(w.cuda(), mode)
     row_counts = ROWS if args.rows is None else [args.rows]
@@ -662,7 +667,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--fp8", choices=["row", "block32"], default=None,
+    ap.add_argument("--fp8", choices=["row", "block32", "block32il"], default=None,
                     help="profiling case: only the FP8 head with fused top-64")
     ap.add_argument("--rows", type=int, default=None, choices=list(range(1, 17)),
                     help="with --fp8: one row count instead of 1/5/10/15")

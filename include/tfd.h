@@ -54,7 +54,20 @@ typedef enum {
   TFD_ERR_TIMEOUT = 6       /* (device status only) a bounded device wait gave up */
 } tfd_status;
 
-typedef enum { TFD_W_BF16 = 0, TFD_W_FP8_ROW = 1, TFD_W_FP8_BLOCK32 = 2 } tfd_wfmt;
+/*
+ * Weight formats. TFD_W_FP8_BLOCK32_IL holds the same codes and scales as TFD_W_FP8_BLOCK32 with
+ * the codes of each row reordered in steps of 64 columns (k % 64 == 0): within step c, bytes
+ * 64c + 16t + 8b + e (t = 0..3, b = 0..1, e = 0..7) hold the code of column 64c + 32b + 8t + e,
+ * so the 8 codes a GEMV thread takes from each of a step's two 32-wide blocks are one 16-byte
+ * load. It is this library's own layout (no counterpart on the pages); tfd_quant_fp8 writes it and
+ * tfd_fp8_block32_relayout converts to and from the plain row-major layout.
+ */
+typedef enum {
+  TFD_W_BF16 = 0,
+  TFD_W_FP8_ROW = 1,
+  TFD_W_FP8_BLOCK32 = 2,
+  TFD_W_FP8_BLOCK32_IL = 3
+} tfd_wfmt;
 typedef enum { TFD_X_BF16 = 0, TFD_X_F32 = 1 } tfd_xfmt;
 typedef enum { TFD_OUT_NONE = 0, TFD_OUT_F32 = 1, TFD_OUT_BF16 = 2, TFD_OUT_ADD_BF16 = 3 } tfd_out;
 
@@ -78,6 +91,8 @@ int tfd_version(void);
  *     smallest power of two with amax <= 448 * 2^e (an all-zero block stores 0); code =
  *     e4m3_rne_sat(w * 2^-(byte - 127)). [DSPARK] "FP8 draft head": E4M3 codes with E8M0 scales in
  *     32x32 blocks.
+ *   mode TFD_W_FP8_BLOCK32_IL: the codes and scales of TFD_W_FP8_BLOCK32, codes written in the
+ *     interleaved layout described at tfd_wfmt (k % 64 == 0).
  *   E4M3 is the "fn" form (bias 7, max 448, 0x7F = NaN); encoding is round-to-nearest-even with
  *   saturation to +-448. Weights must be finite.
  * Args:
@@ -236,6 +251,17 @@ tfd_status tfd_window_attn(const void* q, const void* k_new, const void* v_new,
 tfd_status tfd_accept(const int32_t* drafts, const int32_t* n_asked, const int32_t* draws,
                       int streams, int win, int32_t* n_kept, int64_t* asked_hist,
                       int64_t* kept_hist, int32_t* dev_status, void* stream);
+
+/*
+ * tfd_fp8_block32_relayout - block-32 FP8 codes between the plain row-major layout and the
+ *   interleaved layout of TFD_W_FP8_BLOCK32_IL (a permutation of bytes within each row; the
+ *   scales are unchanged). No counterpart on the pages: it serves codes made elsewhere.
+ * Args:
+ *   in, out device uint8 [n][k], not overlapping; n >= 1; k >= 64 and k % 64 == 0; 16-byte
+ *   aligned. to_interleaved: 1 plain -> interleaved, 0 interleaved -> plain.
+ */
+tfd_status tfd_fp8_block32_relayout(const uint8_t* in, int64_t n, int64_t k, int to_interleaved,
+                                    uint8_t* out, void* stream);
 
 /*
  * tfd_rmsnorm - RMSNorm of hidden rows.

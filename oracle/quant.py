@@ -89,3 +89,23 @@ def dequant_fp8_block32(codes, scale_bytes):
     sc = np.exp2(np.asarray(scale_bytes, dtype=np.float64) - 127.0)
     full = np.repeat(np.repeat(sc, 32, axis=0), 32, axis=1)
     return e4m3_decode(codes) * full
+
+
+def block32_interleave(codes):
+    """Plain row-major block-32 codes [n][k] (k % 64 == 0) -> this library's interleaved layout:
+    in each 64-column step c, byte 64c + 16t + 8b + e holds column 64c + 32b + 8t + e
+    (t = 0..3, b = 0..1, e = 0..7). A layout of this library (the pages fix none); the values are
+    those of quant_fp8_block32."""
+    c = np.asarray(codes)
+    n, k = c.shape
+    if k % 64:
+        raise ValueError("k must be a multiple of 64")
+    # [n][step][b][t][e] -> [n][step][t][b][e]
+    return c.reshape(n, k // 64, 2, 4, 8).transpose(0, 1, 3, 2, 4).reshape(n, k)
+
+
+def block32_deinterleave(codes):
+    """The inverse of block32_interleave."""
+    c = np.asarray(codes)
+    n, k = c.shape
+    return c.reshape(n, k // 64, 4, 2, 8).transpose(0, 1, 3, 2, 4).reshape(n, k)

@@ -41,6 +41,9 @@ namespace {
 #ifndef TFD_GEMV_DEPTH_BLK_NT2
 #define TFD_GEMV_DEPTH_BLK_NT2 4
 #endif
+#ifndef TFD_GEMV_DEPTH_BLKIL_NT2
+#define TFD_GEMV_DEPTH_BLKIL_NT2 4
+#endif
 // Minimum resident blocks per SM asked of the compiler for one n-tile (2 caps registers at 64).
 #ifndef TFD_GEMV_MINB_NT1
 #define TFD_GEMV_MINB_NT1 1
@@ -54,6 +57,7 @@ constexpr int gemv_depth() {
   return (XF == TFD_X_F32 && NT == 2) ? TFD_GEMV_DEPTH_X32_NT2
        : WF == TFD_W_BF16 ? (NT == 1 ? TFD_GEMV_DEPTH_NT1 : TFD_GEMV_DEPTH_NT2)
        : WF == TFD_W_FP8_ROW ? (NT == 1 ? TFD_GEMV_DEPTH_FP8_NT1 : TFD_GEMV_DEPTH_FP8_NT2)
+       : WF == TFD_W_FP8_BLOCK32_IL ? (NT == 1 ? TFD_GEMV_DEPTH_FP8_NT1 : TFD_GEMV_DEPTH_BLKIL_NT2)
                              : (NT == 1 ? TFD_GEMV_DEPTH_FP8_NT1 : TFD_GEMV_DEPTH_BLK_NT2);
 }
 
@@ -72,6 +76,10 @@ struct WTraits<TFD_W_BF16> {  // 8 bf16 per thread-row load (16 B)
 };
 template <>
 struct WTraits<TFD_W_FP8_ROW> {  // 16 codes per thread-row load (16 B)
+  static constexpr int E = 16, WORDS = 4, ELEM_BYTES = 1;
+};
+template <>
+struct WTraits<TFD_W_FP8_BLOCK32_IL> {  // the same 2 x 8 codes, one 16-byte load (interleaved)
   static constexpr int E = 16, WORDS = 4, ELEM_BYTES = 1;
 };
 template <>
@@ -246,6 +254,8 @@ gemv_kernel(const GemvArgs a) {
   // (max |x| in [2^14, 2^15)), which keeps every bf16 activation exact down to 2^-32 of the row's
   // max; the epilogue multiplies by 2^e_r.
   constexpr bool F16 = WF != TFD_W_BF16;
+  // block-32 scales (plain or interleaved codes): each step is two 32-wide blocks
+  constexpr bool BLK = WF == TFD_W_FP8_BLOCK32 || WF == TFD_W_FP8_BLOCK32_IL;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int mt = warp % MT, ks = warp / MT;
@@ -297,7 +307,7 @@ gemv_kernel(const GemvArgs a) {
     rv0 = in && row < N;
     rv1 = in && row + 8 < N;
     lp = wbase + row * row_bytes + ((int64_t)s_begin * STEPK + toff) * EB;
-    if (WF == TFD_W_FP8_BLOCK32) {
+    if (BLK) {
       const int64_t rblk = (ld_g * GR + mt * 16) >> 5;
       rvb = in && rblk * 32 < N;
       sp = blk_scales + rblk * kblocks + 2 * (int64_t)s_begin;
@@ -307,7 +317,7 @@ gemv_kernel(const GemvArgs a) {
   auto issue = [&](WLoad<WF>& b) {
     // the usual step: both rows and (block-32 form) both blocks in range, no zero fill
     const bool full = rv1 && ld_s < (WF == TFD_W_FP8_BLOCK32 ? nvalid_b : nvalid) &&
-                      (WF != TFD_W_FP8_BLOCK32 || sc16);
+                      (!BLK || sc16);
     if (full) {
       if (WF == TFD_W_FP8_BLOCK32) {
         uint2 v = ldg_stream8(lp);
@@ -324,6 +334,7 @@ gemv_kernel(const GemvArgs a) {
         b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
         v = ldg_stream16(lp + 8 * row_bytes);
         b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
+        if (WF == TFD_W_FP8_BLOCK32_IL) b.scb = __ldg(reinterpret_cast<const uint16_t*>(sp));
       }
       lp += STEPK * EB;
       sp += 2;
@@ -360,6 +371,8 @@ gemv_kernel(const GemvArgs a) {
           uint4 v = ldg_stream16(lp + 8 * row_bytes);
           b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
         }
+        // interleaved block-32 (k % 64 == 0): both blocks of a step are in range together
+        if (WF == TFD_W_FP8_BLOCK32_IL && rvb) b.scb = __ldg(reinterpret_cast<const uint16_t*>(sp));
       }
     }
     lp += STEPK * EB;
@@ -423,8 +436,8 @@ gemv_kernel(const GemvArgs a) {
       const int64_t kg = (int64_t)kstep0 * STEPK + k0;  // in the whole row
       // A thread's 16-element chunk is contiguous, except in the block-32 form, where it is 8 elements
       // of each 32-wide scale block of the step (so every MMA stays inside one block).
-      const int tt = WF == TFD_W_FP8_BLOCK32 ? (rem & 31) >> 3 : rem / E;
-      const int hf = WF == TFD_W_FP8_BLOCK32 ? rem >> 5 : (rem - tt * E) >> 3;
+      const int tt = BLK ? (rem & 31) >> 3 : rem / E;
+      const int hf = BLK ? rem >> 5 : (rem - tt * E) >> 3;
       const int ln = (r & 7) * 4 + tt;
       const int nt = r >> 3;
       const bool ok = r < rows && kg < K;
@@ -481,7 +494,7 @@ gemv_kernel(const GemvArgs a) {
   // added to the accumulator times its scale; its activation fragments are read per block, which
   // keeps fewer registers live.
   auto compute = [&](const WLoad<WF>& b, int sg, float (&acc)[NT][4]) {
-    if constexpr (WF == TFD_W_FP8_BLOCK32) {
+    if constexpr (BLK) {
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {
         uint32_t xq[NT][PL][4];
@@ -881,6 +894,7 @@ size_t gemv_smem_any(int wfmt, int xfmt, int rows, int64_t k) {
        : (f32 ? gemv_smem<WF, TFD_X_F32, 1>(k, nullptr) : gemv_smem<WF, TFD_X_BF16, 1>(k, nullptr)))
   if (wfmt == TFD_W_FP8_ROW) return TFD_SMEM(TFD_W_FP8_ROW);
   if (wfmt == TFD_W_FP8_BLOCK32) return TFD_SMEM(TFD_W_FP8_BLOCK32);
+  if (wfmt == TFD_W_FP8_BLOCK32_IL) return TFD_SMEM(TFD_W_FP8_BLOCK32_IL);
   return TFD_SMEM(TFD_W_BF16);
 #undef TFD_SMEM
 }
@@ -938,7 +952,7 @@ extern "C" int64_t tfd_head_gemv_max_k(int rows, int xfmt) {
   int64_t best = 0;
   for (int64_t k = 256; k <= (1 << 20); k += 256) {
     bool ok = true;
-    for (int wf = 0; wf < 3 && ok; ++wf) ok = gemv_smem_any(wf, xfmt, rows, k) <= kSmemLimit;
+    for (int wf = 0; wf < 4 && ok; ++wf) ok = gemv_smem_any(wf, xfmt, rows, k) <= kSmemLimit;
     if (!ok) break;
     best = k;
   }
@@ -954,13 +968,14 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   using tfd_host::aligned;
   (void)dev_status;  // no device-data errors are possible in this call
   if (!w || !x) return TFD_ERR_INVALID;
-  if (wfmt < TFD_W_BF16 || wfmt > TFD_W_FP8_BLOCK32) return TFD_ERR_INVALID;
+  if (wfmt < TFD_W_BF16 || wfmt > TFD_W_FP8_BLOCK32_IL) return TFD_ERR_INVALID;
   if (xfmt != TFD_X_BF16 && xfmt != TFD_X_F32) return TFD_ERR_INVALID;
   if (out_mode < TFD_OUT_NONE || out_mode > TFD_OUT_ADD_BF16) return TFD_ERR_INVALID;
   if (rows < 1 || rows > TFD_MAX_ROWS) return TFD_ERR_INVALID;
   if (n < 1 || n > (int64_t)INT32_MAX || k < 16 || k % 16 != 0) return TFD_ERR_INVALID;
   if (wfmt != TFD_W_BF16 && !w_scales) return TFD_ERR_INVALID;
   if (wfmt == TFD_W_FP8_BLOCK32 && (n % 32 != 0 || k % 32 != 0)) return TFD_ERR_INVALID;
+  if (wfmt == TFD_W_FP8_BLOCK32_IL && (n % 32 != 0 || k % 64 != 0)) return TFD_ERR_INVALID;
   const size_t xb = xfmt == TFD_X_F32 ? 4 : 2;
   if (ldx < k || ((size_t)ldx * xb) % 16 != 0) return TFD_ERR_INVALID;
   if (!aligned(w, 16) || !aligned(x, 16)) return TFD_ERR_INVALID;
@@ -1007,6 +1022,8 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   tfd_status st;
   if (wfmt == TFD_W_FP8_ROW) st = gemv_launch_x<TFD_W_FP8_ROW>(a, xfmt, parts, s);
   else if (wfmt == TFD_W_FP8_BLOCK32) st = gemv_launch_x<TFD_W_FP8_BLOCK32>(a, xfmt, parts, s);
+  else if (wfmt == TFD_W_FP8_BLOCK32_IL)
+    st = gemv_launch_x<TFD_W_FP8_BLOCK32_IL>(a, xfmt, parts, s);
   else st = gemv_launch_x<TFD_W_BF16>(a, xfmt, parts, s);
   if (st != TFD_OK || topk <= 1) return st;
   return tfd_internal::topk_launch(a.logits, rows, n, a.ld_logits, topk, id_map, top_vals, top_ids,

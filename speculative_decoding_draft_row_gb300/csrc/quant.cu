@@ -60,7 +60,9 @@ __global__ void __launch_bounds__(256) quant_row_kernel(const uint16_t* __restri
   }
 }
 
-// Block of 32 rows x 256 columns (8 scale blocks); thread = (row, 32-column block).
+// Block of 32 rows x 256 columns (8 scale blocks); thread = (row, 32-column block). IL: the codes
+// go to the interleaved layout (piece t of block b of 64-column step c at 64c + 16t + 8b).
+template <bool IL>
 __global__ void __launch_bounds__(256) quant_block_kernel(const uint16_t* __restrict__ w,
                                                           int64_t n, int64_t k,
                                                           uint8_t* __restrict__ codes,
@@ -115,9 +117,41 @@ __global__ void __launch_bounds__(256) quant_block_kernel(const uint16_t* __rest
     float a2 = bf16_lo(u[2 * i + 1]) * inv, a3 = bf16_hi(u[2 * i + 1]) * inv;
     out[i] = e4m3x2(a0, a1) | (e4m3x2(a2, a3) << 16);
   }
-  uint4* cp = reinterpret_cast<uint4*>(codes + row * k + col0);
-  cp[0] = make_uint4(out[0], out[1], out[2], out[3]);
-  cp[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  if (IL) {
+    uint8_t* rp = codes + row * k + (col0 & ~(int64_t)63) + 8 * ((col0 >> 5) & 1);
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      *reinterpret_cast<uint2*>(rp + 16 * t) = make_uint2(out[2 * t], out[2 * t + 1]);
+  } else {
+    uint4* cp = reinterpret_cast<uint4*>(codes + row * k + col0);
+    cp[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    cp[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+}
+
+// One thread per 16 bytes of interleaved layout: piece t of 64-column step c, i.e. plain bytes
+// 64c + 8t .. +8 (block 0) and 64c + 32 + 8t .. +8 (block 1).
+__global__ void __launch_bounds__(256) relayout_kernel(const uint8_t* __restrict__ in, int64_t n,
+                                                       int64_t k, bool to_il,
+                                                       uint8_t* __restrict__ out) {
+  const int64_t per_row = k / 16;
+  const int64_t total = n * per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / per_row, q = i - row * per_row;
+    const int64_t c = q >> 2, t = q & 3;
+    const int64_t il = row * k + 64 * c + 16 * t;
+    const int64_t p0 = row * k + 64 * c + 8 * t, p1 = p0 + 32;
+    if (to_il) {
+      const uint2 a = *reinterpret_cast<const uint2*>(in + p0);
+      const uint2 b = *reinterpret_cast<const uint2*>(in + p1);
+      *reinterpret_cast<uint4*>(out + il) = make_uint4(a.x, a.y, b.x, b.y);
+    } else {
+      const uint4 v = *reinterpret_cast<const uint4*>(in + il);
+      *reinterpret_cast<uint2*>(out + p0) = make_uint2(v.x, v.y);
+      *reinterpret_cast<uint2*>(out + p1) = make_uint2(v.z, v.w);
+    }
+  }
 }
 
 }  // namespace
@@ -135,12 +169,32 @@ extern "C" tfd_status tfd_quant_fp8(const void* w_bf16, int64_t n, int64_t k, in
                                          reinterpret_cast<float*>(scales));
     return tfd_host::launch_status();
   }
-  if (mode == TFD_W_FP8_BLOCK32) {
-    if (n % 32 != 0 || k % 32 != 0 || n / 32 > 65535) return TFD_ERR_INVALID;
+  if (mode == TFD_W_FP8_BLOCK32 || mode == TFD_W_FP8_BLOCK32_IL) {
+    const bool il = mode == TFD_W_FP8_BLOCK32_IL;
+    if (n % 32 != 0 || k % (il ? 64 : 32) != 0 || n / 32 > 65535) return TFD_ERR_INVALID;
     dim3 grid((unsigned)((k + 255) / 256), (unsigned)(n / 32));
-    quant_block_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint16_t*>(w_bf16), n, k, codes,
-                                           reinterpret_cast<uint8_t*>(scales));
+    auto kern = il ? quant_block_kernel<true> : quant_block_kernel<false>;
+    kern<<<grid, 256, 0, s>>>(reinterpret_cast<const uint16_t*>(w_bf16), n, k, codes,
+                              reinterpret_cast<uint8_t*>(scales));
     return tfd_host::launch_status();
   }
   return TFD_ERR_INVALID;
+}
+
+extern "C" tfd_status tfd_fp8_block32_relayout(const uint8_t* in, int64_t n, int64_t k,
+                                               int to_interleaved, uint8_t* out, void* stream) {
+  using tfd_host::aligned;
+  if (!in || !out || n < 1 || k < 64 || k % 64 != 0) return TFD_ERR_INVALID;
+  if (to_interleaved != 0 && to_interleaved != 1) return TFD_ERR_INVALID;
+  if (!aligned(in, 16) || !aligned(out, 16)) return TFD_ERR_INVALID;
+  const uintptr_t a = (uintptr_t)in, b = (uintptr_t)out, len = (uintptr_t)(n * k);
+  if (a < b + len && b < a + len) return TFD_ERR_INVALID;
+  const int64_t total = n * (k / 16);
+  int sms = tfd_host::sm_count();
+  if (sms < 1) sms = 1;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+  relayout_kernel<<<(unsigned)blocks, 256, 0, tfd_host::as_stream(stream)>>>(
+      in, n, k, to_interleaved == 1, out);
+  return tfd_host::launch_status();
 }

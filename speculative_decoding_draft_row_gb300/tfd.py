@@ -13,7 +13,7 @@ import torch
 from . import build as _build
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_DATA, ERR_TIMEOUT = range(7)
-W_BF16, W_FP8_ROW, W_FP8_BLOCK32 = 0, 1, 2
+W_BF16, W_FP8_ROW, W_FP8_BLOCK32, W_FP8_BLOCK32_IL = 0, 1, 2, 3
 X_BF16, X_F32 = 0, 1
 OUT_NONE, OUT_F32, OUT_BF16, OUT_ADD_BF16 = 0, 1, 2, 3
 MAX_ROWS, MAX_TOPK, MAX_WINDOW = 16, 512, 511
@@ -39,6 +39,7 @@ SIGNATURES = {
     "tfd_window_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _f32, _f32, _vp, _vp, _vp, _i32, _i32,
                                _i32, _i32, _i32, _vp, _vp, _vp]),
     "tfd_accept": (_i32, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "tfd_fp8_block32_relayout": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp]),
     "tfd_rmsnorm": (_i32, [_vp, _i64, _vp, _f32, _i32, _i64, _vp, _i64, _vp]),
     "tfd_swiglu": (_i32, [_vp, _vp, _i64, _i32, _i64, _vp, _i64, _vp]),
     "tfd_absorb": (_i32, [_vp, _vp, _vp, _f32, _f32, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
@@ -108,8 +109,9 @@ def zeroed_workspace(nbytes, device=None):
 # ---- entry points ---------------------------------------------------------------------------
 
 def tfd_quant_fp8(w, mode, codes=None, scales=None, stream=None):
-    """FP8 codes of a bf16 weight [n][k]: mode W_FP8_ROW (float scales [n]) or W_FP8_BLOCK32
-    (uint8 scales [n/32][k/32]). Returns (codes, scales)."""
+    """FP8 codes of a bf16 weight [n][k]: mode W_FP8_ROW (float scales [n]), W_FP8_BLOCK32 or
+    W_FP8_BLOCK32_IL (uint8 scales [n/32][k/32]; IL writes the interleaved code layout).
+    Returns (codes, scales)."""
     _dev(w)
     n, k = w.shape
     if codes is None:
@@ -303,3 +305,15 @@ def tfd_absorb(k_rows, v_rows, p0, k_ring, v_ring, k_gamma=None, eps=1e-6, rope_
                               _p(p0), n, _p(k_ring), _p(v_ring), ring, streams, heads, dim,
                               _p(dev_status), _stream(stream))
     _check("tfd_absorb", st)
+
+
+def tfd_fp8_block32_relayout(codes, to_interleaved=True, out=None, stream=None):
+    """Block-32 FP8 codes [n][k] between the plain and the interleaved layout. Returns out."""
+    _dev(codes, out)
+    n, k = codes.shape
+    if out is None:
+        out = torch.empty_like(codes)
+    st = library().tfd_fp8_block32_relayout(_p(codes), n, k, 1 if to_interleaved else 0, _p(out),
+                                            _stream(stream))
+    _check("tfd_fp8_block32_relayout", st)
+    return out

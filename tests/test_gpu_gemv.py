@@ -118,6 +118,35 @@ def test_fused_topk_matches_own_logits_and_oracle(wfmt):
         assert_topk_valid(np32(tv), ti.cpu().numpy(), acc, S, k, what=f"top-{k}")
 
 
+@pytest.mark.parametrize("n,k,rows,xf32", [(4096, 4096, 1, False), (4096, 4096, 10, False),
+                                           (2080, 1088, 16, False), (2048, 512, 7, True)])
+def test_block32_interleaved_equals_plain_bit_for_bit(n, k, rows, xf32):
+    """The interleaved block-32 layout changes only how the codes are loaded: logits and top-k
+    are bit-identical to the plain layout's."""
+    need_gpu()
+    case = make_case(n, k, rows, tfd.W_FP8_BLOCK32, xf32, tid=350)
+    il = tfd.tfd_fp8_block32_relayout(case["w"], True)
+    y0, v0, i0 = tfd.tfd_head_gemv(case["w"], tfd.W_FP8_BLOCK32, case["scales"], case["x"],
+                                   tfd.OUT_F32, topk=16)
+    y1, v1, i1 = tfd.tfd_head_gemv(il, tfd.W_FP8_BLOCK32_IL, case["scales"], case["x"],
+                                   tfd.OUT_F32, topk=16)
+    torch.cuda.synchronize()
+    assert same_bits(np32(y0), np32(y1)) and torch.equal(i0, i1) and same_bits(np32(v0), np32(v1))
+    acc, S = oracle_acc_S(case, tfd.W_FP8_BLOCK32)
+    assert_fp32_close(np32(y1), acc, S, "interleaved block-32 logits")
+
+
+def test_fused_topk_over_a_long_ragged_vocabulary():
+    """270016 logits a row (not a multiple of 8 x 16): the fused top-k from the GEMV's sub-group
+    maxima, ragged parts at the end of the row."""
+    need_gpu()
+    case = make_case(270016, 64, 3, tfd.W_BF16, tid=360, tie_frac=0.01)
+    y, tv, ti = tfd.tfd_head_gemv(case["w"], tfd.W_BF16, None, case["x"], tfd.OUT_F32, topk=100)
+    torch.cuda.synchronize()
+    ov, oi = oracle_topk(np32(y), 100)
+    assert np.array_equal(ti.cpu().numpy(), oi) and same_bits(np32(tv), ov)
+
+
 def test_fused_topk_with_one_k_slice():
     """The short-k, many-row form (one k-slice per block, 256-row groups) with a fused top-64."""
     need_gpu()

@@ -93,3 +93,24 @@ def test_full_head_sampled_rows(mode):
         s_gpu = scales[torch.from_numpy(blocks).cuda()].cpu().numpy()
         assert np.array_equal(s_gpu, os_)
     assert np.array_equal(c_gpu, oc)
+
+
+def test_block32_interleaved_codes_and_relayout():
+    """Mode W_FP8_BLOCK32_IL: the plain block-32 codes in the interleaved layout, same scales; the
+    relayout converts either way."""
+    need_gpu()
+    from oracle.quant import block32_interleave
+    w = inputs.normal_bf16((256, 4096 + 64), 0.02, 995)
+    wd = w.cuda()
+    plain, sp = tfd.tfd_quant_fp8(wd, tfd.W_FP8_BLOCK32)
+    il, si = tfd.tfd_quant_fp8(wd, tfd.W_FP8_BLOCK32_IL)
+    to_il = tfd.tfd_fp8_block32_relayout(plain, True)
+    back = tfd.tfd_fp8_block32_relayout(il, False)
+    torch.cuda.synchronize()
+    oc, os_ = quant_fp8_block32(w.float().numpy())
+    assert np.array_equal(plain.cpu().numpy(), oc) and np.array_equal(sp.cpu().numpy(), os_)
+    assert np.array_equal(il.cpu().numpy(), block32_interleave(oc))
+    assert np.array_equal(si.cpu().numpy(), os_)
+    assert torch.equal(to_il, il) and torch.equal(back, plain)
+    with pytest.raises(tfd.TfdError):
+        tfd.tfd_quant_fp8(inputs.normal_bf16((64, 96), 0.02, 996).cuda(), tfd.W_FP8_BLOCK32_IL)

@@ -4,6 +4,7 @@ import json
 import os
 
 import numpy as np
+import pytest
 import torch
 
 from oracle.numerics import E4M3_DECODE, e4m3_decode
@@ -138,3 +139,23 @@ def test_block_storage_size_matches_page():
     assert f["codes_bytes"] + f["scale_bytes"] == f["total_bytes"]
     assert round(f["total_bytes"] / 1e9, 2) == f["page_gb"]
     assert E4M3_DECODE[0x7E] == 448.0
+
+
+def test_block32_interleaved_layout_worked_example_and_round_trip():
+    """The interleaved layout on a row whose code equals its column: each 16-byte piece holds
+    8 columns of the first 32-wide block, then the same 8 of the second (hand-written)."""
+    from oracle.quant import block32_deinterleave, block32_interleave
+    row = np.arange(128).reshape(1, 128)
+    want = ([0, 1, 2, 3, 4, 5, 6, 7, 32, 33, 34, 35, 36, 37, 38, 39,
+             8, 9, 10, 11, 12, 13, 14, 15, 40, 41, 42, 43, 44, 45, 46, 47,
+             16, 17, 18, 19, 20, 21, 22, 23, 48, 49, 50, 51, 52, 53, 54, 55,
+             24, 25, 26, 27, 28, 29, 30, 31, 56, 57, 58, 59, 60, 61, 62, 63])
+    got = block32_interleave(row)[0].tolist()
+    assert got[:64] == want
+    assert got[64:] == [v + 64 for v in want]
+    codes = np.random.default_rng([0, 990, 0]).integers(0, 256, size=(96, 320)).astype(np.uint8)
+    il = block32_interleave(codes)
+    assert np.array_equal(block32_deinterleave(il), codes)
+    assert not np.array_equal(il, codes)
+    with pytest.raises(ValueError):
+        block32_interleave(codes[:, :96])

@@ -344,9 +344,11 @@ def run_ours(args):
 
     # ---- FP8 head, fused top-64 (reported beside the headline) ----
     fp8 = {}
-    for mode, name in ((tfd.W_FP8_BLOCK32, "e4m3_e8m0_32x32"),
-                       (tfd.W_FP8_BLOCK32_IL, "e4m3_e8m0_32x32_interleaved"),
-                       (tfd.W_FP8_ROW, "e4m3_row")):
+    for mode, name, aq in ((tfd.W_FP8_BLOCK32, "e4m3_e8m0_32x32", False),
+                           (tfd.W_FP8_BLOCK32_IL, "e4m3_e8m0_32x32_interleaved", False),
+                           (tfd.W_FP8_ROW, "e4m3_row", False),
+                           (tfd.W_FP8_BLOCK32_IL, "e4m3_e8m0_32x32_interleaved_w8a8", True),
+                           (tfd.W_FP8_ROW, "e4m3_row_w8a8", True)):
         codes, scales = tfd.tfd_quant_fp8(wd, mode)
         ws64 = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(16, VOCAB, 64))
         out = {}
@@ -354,7 +356,7 @@ def run_ours(args):
             v64 = torch.empty((r, 64), dtype=torch.float32, device="cuda")
             i64 = torch.empty((r, 64), dtype=torch.int32, device="cuda")
             f = lambda: tfd.tfd_head_gemv(codes, mode, scales, xs[r], tfd.OUT_NONE, topk=64,
-                                          top_vals=v64, top_ids=i64, ws=ws64)
+                                          top_vals=v64, top_ids=i64, ws=ws64, act_e4m3=aq)
             for _ in range(3):
                 f()
             ms = time_graph(f, 20)
@@ -555,13 +557,14 @@ def run_fp8_case(args):
         v = torch.empty((r, 64), dtype=torch.float32, device="cuda")
         i = torch.empty((r, 64), dtype=torch.int32, device="cuda")
         f = lambda: tfd.tfd_head_gemv(codes, mode, scales, xs[r], tfd.OUT_NONE, topk=64,
-                                      top_vals=v, top_ids=i, ws=ws)
+                                      top_vals=v, top_ids=i, ws=ws, act_e4m3=args.w8a8)
         for _ in range(args.warmup):
             f()
         ms = time_graph(f, args.steps)
         out[str(r)] = {"us": round(ms * 1e3, 2),
                        "gbs": round(fp8_call_bytes(r) / (ms * 1e-3) / 1e9, 1)}
-    print(json.dumps({"case": f"fp8 {args.fp8} top-64", "per_rows": out}), flush=True)
+    print(json.dumps({"case": f"fp8 {args.fp8}{' w8a8' if args.w8a8 else ''} top-64",
+                      "per_rows": out}), flush=True)
 
 
 def run_case(args):
@@ -671,6 +674,8 @@ def main():
                     help="profiling case: only the FP8 head with fused top-64")
     ap.add_argument("--rows", type=int, default=None, choices=list(range(1, 17)),
                     help="with --fp8: one row count instead of 1/5/10/15")
+    ap.add_argument("--w8a8", action="store_true",
+                    help="with --fp8: quantise the activation rows to E4M3 in the call")
     ap.add_argument("--case", choices=["attn", "rescore", "topk64", "topk512", "twostage"],
                     default=None,
                     help="profiling case: one row of the path alone")

@@ -68,7 +68,13 @@ typedef enum {
   TFD_W_FP8_BLOCK32 = 2,
   TFD_W_FP8_BLOCK32_IL = 3
 } tfd_wfmt;
-typedef enum { TFD_X_BF16 = 0, TFD_X_F32 = 1 } tfd_xfmt;
+/*
+ * Activation formats. TFD_X_BF16_E4M3 (FP8 weights only, W8A8): bf16 activations quantised per
+ * row inside the call by the weights' row rule, s_r = fl32(amax_r / 448), code = e4m3_rne_sat(
+ * fl32(x / s_r)) (a zero row keeps its zeros), and multiplied on the E4M3 tensor-core path; the
+ * result is acc * s_r (* the weights' scales) with fp32 accumulation.
+ */
+typedef enum { TFD_X_BF16 = 0, TFD_X_F32 = 1, TFD_X_BF16_E4M3 = 2 } tfd_xfmt;
 typedef enum { TFD_OUT_NONE = 0, TFD_OUT_F32 = 1, TFD_OUT_BF16 = 2, TFD_OUT_ADD_BF16 = 3 } tfd_out;
 
 /* Limits from the pages' statement of the problem. */
@@ -119,7 +125,8 @@ tfd_status tfd_quant_fp8(const void* w_bf16, int64_t n, int64_t k, int mode, uin
  *   n, k     outputs per row (>= 1) and reduction length (k >= 16, k % 16 == 0; BLOCK32 also
  *            n % 32 == 0 and k % 32 == 0).
  *   x        device: bf16 or float (xfmt) [rows][ldx], ldx >= k. Float activations are used at
- *            full fp32 precision.
+ *            full fp32 precision; TFD_X_BF16_E4M3 (FP8 weights only) quantises bf16 rows to E4M3
+ *            first (W8A8, see tfd_xfmt).
  *   rows     1..16.
  *   out_mode NONE: no output; F32: y float [rows][ldy] = fl32(acc); BF16: y bf16 = bf16(fl32(acc));
  *            ADD_BF16: y bf16 is read as the residual and overwritten with bf16(res + acc), which

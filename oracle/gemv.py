@@ -9,12 +9,14 @@ every bf16 x bf16, e4m3 x bf16 and bf16 x fp32 product is exact, so ``acc`` is t
 to float64 rounding; the oracle then rounds only where the method rounds.
 
 Reading (the pages do not say whether the FP8 path quantises activations): activations stay bf16
-(or fp32) and only weights are FP8 (W8A16), with fp32 accumulation.
+(or fp32) and only weights are FP8 (W8A16), with fp32 accumulation. The W8A8 form (DSpark FP8 head
+page: the Metal pass keeps "act_quant rows") quantises each activation row by the weights' row rule
+(s = fl32(amax / 448), code = e4m3(fl32(x / s))) and multiplies the decoded values exactly.
 """
 import numpy as np
 
 from .numerics import fl32, round_bf16
-from .quant import dequant_fp8_block32, dequant_fp8_row
+from .quant import dequant_fp8_block32, dequant_fp8_row, quant_fp8_row
 
 W_BF16, W_FP8_ROW, W_FP8_BLOCK32 = 0, 1, 2
 OUT_NONE, OUT_F32, OUT_BF16, OUT_ADD_BF16 = 0, 1, 2, 3
@@ -31,27 +33,36 @@ def weights_f64(w, wfmt, scales=None):
     raise ValueError(wfmt)
 
 
-def gemv_acc(w, x, wfmt=W_BF16, scales=None):
-    """float64 ``acc[r][n]`` for x [R][K] against W [N][K] (codes for the FP8 forms)."""
+def act_e4m3(x):
+    """Activation rows after the W8A8 quantisation: the exact values s_r * dec(code) (float64)."""
+    codes, s = quant_fp8_row(np.atleast_2d(np.asarray(x, dtype=np.float32)))
+    return dequant_fp8_row(codes, s)
+
+
+def gemv_acc(w, x, wfmt=W_BF16, scales=None, act_fp8=False):
+    """float64 ``acc[r][n]`` for x [R][K] against W [N][K] (codes for the FP8 forms); act_fp8
+    quantises the activation rows first (W8A8)."""
     wd = weights_f64(w, wfmt, scales)
-    return np.asarray(x, dtype=np.float64) @ wd.T
+    xv = act_e4m3(x) if act_fp8 else np.asarray(x, dtype=np.float64)
+    return xv @ wd.T
 
 
-def gemv_abs_scale(w, x, wfmt=W_BF16, scales=None):
+def gemv_abs_scale(w, x, wfmt=W_BF16, scales=None, act_fp8=False):
     """``S[r][n] = sum_k |W[n][k] * x[r][k]|``: the magnitude that bounds the rounding error of an
     fp32 dot product; the fp32-accumulation tolerance is stated relative to it."""
     wd = np.abs(weights_f64(w, wfmt, scales))
-    return np.abs(np.asarray(x, dtype=np.float64)) @ wd.T
+    xv = act_e4m3(x) if act_fp8 else np.asarray(x, dtype=np.float64)
+    return np.abs(xv) @ wd.T
 
 
-def gemv(w, x, wfmt=W_BF16, scales=None, out_mode=OUT_F32, res=None):
+def gemv(w, x, wfmt=W_BF16, scales=None, out_mode=OUT_F32, res=None, act_fp8=False):
     """The GEMV's output in the requested mode.
 
     F32: ``fl32(acc)``. BF16: ``bf16(fl32(acc))`` (fp32 sums, then the output cast).
     ADD_BF16: ``bf16(res + acc)``, one rounding of the exact sum (the residual add "rounded once").
     NONE: returns None.
     """
-    acc = gemv_acc(w, x, wfmt, scales)
+    acc = gemv_acc(w, x, wfmt, scales, act_fp8)
     if out_mode == OUT_NONE:
         return None
     if out_mode == OUT_F32:

@@ -1,0 +1,973 @@
+// gemv_kernel.cuh - the few-row vocabulary-head GEMV kernel (bf16, FP8 row-scaled, FP8
+// 32x32-block-scaled weights) fused with the output modes and a split-vocabulary top-1, and its
+// launchers. Each weight format's kernels are instantiated in a translation unit of their own
+// (gemv_w*.cu) so they compile in parallel; gemv.cu holds the C entry points.
+//
+// Follows the TFE draft head page (#42), commit "pass kernels and FP8 linears": GEMV over bf16 and
+// e4m3 weights for up to 16 rows, out bf16 / fp32 / added to bf16, and the top-1 of a vocabulary
+// row in parts and a join; the DSpark FP8 head page (#3296), "FP8 draft head": E4M3 codes with
+// E8M0 scales in 32x32 blocks, the drafter's top 64 candidates.
+//
+// Design (GB300, HBM-bound): a 1..16-row GEMV reads every weight byte once, so the kernel is a
+// weight stream. Each block is persistent and owns a contiguous range of 64-row groups (one
+// "part" of the vocabulary). Its 16 warps split a group as 4 row tiles x 4 k slices; every warp
+// streams its 16 rows x k-slice straight from HBM into registers with 16-byte (FP8 block form:
+// 8-byte) non-allocating loads kept D steps ahead, and feeds them to warp-level bf16 tensor-core
+// MMAs (m16n8k16, fp32 accumulate) whose other operand is the activation tile held in shared
+// memory in fragment order (conflict-free 16-byte reads). The MMA removes the per-element FMA
+// work that would otherwise cap the CUDA cores at 10-16 rows; FP8 codes are widened to bf16 in
+// registers (exact). The k order inside a dot product is permuted consistently between weights
+// and activations so that each thread's 16 contiguous bytes are one MMA operand chunk.
+// Per group, the four k-slice partials are summed in a fixed order in shared memory, so every
+// output's arithmetic is independent of its index and of the part count.
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+
+namespace tfd_gemv {
+
+// Weight loads kept in flight per warp, in steps, for one and two n-tiles (tuning macros); the
+// FP8 forms have their own two-n-tile depth (their decode needs more registers).
+#ifndef TFD_GEMV_DEPTH_NT1
+#define TFD_GEMV_DEPTH_NT1 4
+#endif
+#ifndef TFD_GEMV_DEPTH_NT2
+#define TFD_GEMV_DEPTH_NT2 8
+#endif
+#ifndef TFD_GEMV_DEPTH_FP8_NT1
+#define TFD_GEMV_DEPTH_FP8_NT1 4
+#endif
+#ifndef TFD_GEMV_DEPTH_FP8_NT2
+#define TFD_GEMV_DEPTH_FP8_NT2 8
+#endif
+#ifndef TFD_GEMV_DEPTH_BLK_NT2
+#define TFD_GEMV_DEPTH_BLK_NT2 4
+#endif
+#ifndef TFD_GEMV_DEPTH_BLKIL_NT2
+#define TFD_GEMV_DEPTH_BLKIL_NT2 4
+#endif
+// Minimum resident blocks per SM asked of the compiler for one n-tile (2 caps registers at 64).
+#ifndef TFD_GEMV_MINB_NT1
+#define TFD_GEMV_MINB_NT1 1
+#endif
+// fp32 activations take three planes of MMA operands; their two-n-tile form keeps a shallower ring
+#ifndef TFD_GEMV_DEPTH_X32_NT2
+#define TFD_GEMV_DEPTH_X32_NT2 4
+#endif
+// W8A8 with two n-tiles
+#ifndef TFD_GEMV_DEPTH_AQ_NT2
+#define TFD_GEMV_DEPTH_AQ_NT2 4
+#endif
+template <int WF, int NT, int XF = TFD_X_BF16>
+constexpr int gemv_depth() {
+  return (XF == TFD_X_F32 && NT == 2) ? TFD_GEMV_DEPTH_X32_NT2
+       : (XF == TFD_X_BF16_E4M3 && NT == 2 && WF == TFD_W_FP8_ROW) ? TFD_GEMV_DEPTH_AQ_NT2
+       : WF == TFD_W_BF16 ? (NT == 1 ? TFD_GEMV_DEPTH_NT1 : TFD_GEMV_DEPTH_NT2)
+       : WF == TFD_W_FP8_ROW ? (NT == 1 ? TFD_GEMV_DEPTH_FP8_NT1 : TFD_GEMV_DEPTH_FP8_NT2)
+       : WF == TFD_W_FP8_BLOCK32_IL ? (NT == 1 ? TFD_GEMV_DEPTH_FP8_NT1 : TFD_GEMV_DEPTH_BLKIL_NT2)
+                             : (NT == 1 ? TFD_GEMV_DEPTH_FP8_NT1 : TFD_GEMV_DEPTH_BLK_NT2);
+}
+
+using namespace tfd;
+
+constexpr int kThreads = 512;
+constexpr int kWarps = 16;
+constexpr int kMaxParts = 1024;
+constexpr int kMaxRowsPad = 16;
+
+template <int WF>
+struct WTraits;
+template <>
+struct WTraits<TFD_W_BF16> {  // 8 bf16 per thread-row load (16 B)
+  static constexpr int E = 8, WORDS = 4, ELEM_BYTES = 2;
+};
+template <>
+struct WTraits<TFD_W_FP8_ROW> {  // 16 codes per thread-row load (16 B)
+  static constexpr int E = 16, WORDS = 4, ELEM_BYTES = 1;
+};
+template <>
+struct WTraits<TFD_W_FP8_BLOCK32_IL> {  // the same 2 x 8 codes, one 16-byte load (interleaved)
+  static constexpr int E = 16, WORDS = 4, ELEM_BYTES = 1;
+};
+template <>
+struct WTraits<TFD_W_FP8_BLOCK32> {  // 2 x 8 codes: 8 from each of the step's two 32-wide blocks
+  static constexpr int E = 16, WORDS = 4, ELEM_BYTES = 1;
+};
+
+struct GemvArgs {
+  const void* w;
+  const void* scales;
+  int64_t n, k;
+  const void* x;
+  int64_t ldx;
+  int rows;
+  int out_mode;
+  void* y;
+  int64_t ldy;
+  int topk;
+  const int32_t* id_map;
+  float* logits;  // fp32 logits destination for topk > 1 (may equal y), else null
+  int64_t ld_logits;
+  uint32_t* submax;  // topk > 1: [rows][ceil(n / 16)] value key of each 16-row sub-group's max
+  uint64_t* part_keys;  // [parts][16]
+  uint32_t* counter;
+  float* top_vals;
+  int32_t* top_ids;
+  int64_t ldt;  // row stride of top_vals / top_ids
+  float* top1_conf;  // [rows] softmax probability of the top-1, or null
+  float2* part_ms;   // [parts][16] per part (max, sum of exp(l - max)) for the confidence
+  int parts;
+  int64_t ngroups;
+  int ssl;  // steps per k slice
+  int csplit;  // blocks of a cluster splitting k (1: no cluster); parts counts clusters
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// d = A B (a zero accumulator input): starts a block's partial sum without zeroing registers.
+__device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                uint32_t a2, uint32_t a3, uint32_t b0,
+                                                uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// d = A B for E4M3 operands (k = 32), fp32 accumulators starting at zero.
+__device__ __forceinline__ void mma_e4m3_16832_z(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, uint32_t b0,
+                                                 uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Two floats -> two E4M3 codes (byte 0 = lo, byte 1 = hi), RNE, saturating to +-448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four E4M3 codes -> two f16x2 words (codes 0,1 and codes 2,3). Every E4M3 value is an f16 value,
+// so the hardware conversion is exact; one instruction widens two codes.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(v));
+}
+
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float f) {
+  return __half_as_ushort(__float2half_rn(f));
+}
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t b) {
+  return __half2float(__ushort_as_half(b));
+}
+
+// Merge of two online-softmax states (max, sum of exp(v - max)).
+__device__ __forceinline__ float2 ms_merge(float2 a, float2 b) {
+  const float m = fmaxf(a.x, b.x);
+  if (m == -INFINITY) return make_float2(-INFINITY, 0.0f);
+  return make_float2(m, a.y * expf(a.x - m) + b.y * expf(b.x - m));
+}
+
+__device__ __forceinline__ float e8m0_scale(uint32_t byte) {
+  return byte == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(byte << 23);
+}
+
+template <int WF>
+struct WLoad {
+  uint32_t r[2][WTraits<WF>::WORDS];  // rows g and g + 8
+  uint32_t scb;                       // the step's two E8M0 scale bytes (FP8_BLOCK32): A | B << 8
+};
+
+// An fp32 value split into three parts of the MMA operand type (bf16 for bf16 weights, f16 for
+// FP8 weights): hi + mid + lo carries every bit of a normal fp32 value.
+template <bool F16>
+__device__ __forceinline__ void split3(float v, uint16_t& h0, uint16_t& h1, uint16_t& h2) {
+  if (F16) {
+    h0 = f32_to_f16_bits(v);
+    float r1 = v - f16_bits_to_f32(h0);
+    h1 = f32_to_f16_bits(r1);
+    float r2 = r1 - f16_bits_to_f32(h1);
+    h2 = f32_to_f16_bits(r2);
+  } else {
+    h0 = f32_to_bf16_bits(v);
+    float r1 = v - bf16_bits_to_f32(h0);
+    h1 = f32_to_bf16_bits(r1);
+    float r2 = r1 - bf16_bits_to_f32(h1);
+    h2 = f32_to_bf16_bits(r2);
+  }
+}
+
+// KSL = k-slices per block: 4 (16 warps = 4 row tiles x 4 k-slices, 64-row groups) or 1 (16 row
+// tiles over the whole k range, 256-row groups: for short k, where 4 slices would leave each warp
+// only a step or two per group).
+template <int WF, int XF, int NT, int KSL = 4>
+struct Layout {
+  static constexpr int E = WTraits<WF>::E;
+  static constexpr bool AQ = XF == TFD_X_BF16_E4M3;  // activations as E4M3 codes (W8A8)
+  static constexpr int H = AQ ? 1 : E / 8;           // 16-byte x chunks per (step, nt) per lane
+  static constexpr int PL = XF == TFD_X_F32 ? 3 : 1; // activation planes
+  static constexpr int MT = 16 / KSL;                // row tiles per block
+  __host__ __device__ static size_t x_bytes(int ssl) {
+    return (size_t)PL * KSL * ssl * NT * H * 32 * 16;
+  }
+  __host__ __device__ static size_t red_bytes() {
+    return KSL == 1 ? 0 : (size_t)2 * kWarps * NT * 32 * 16;
+  }
+  __host__ __device__ static size_t best_bytes() {
+    // block best keys, join keys, per-row x max and x scale, block (max, sum) pairs, join pairs
+    return (size_t)MT * 16 * 8 + 16 * kWarps * 8 + 2 * 16 * 4 + MT * 16 * 8 + 16 * kWarps * 8;
+  }
+  // group partials of a block for its cluster leader, double-buffered (4 k-slices only)
+  __host__ __device__ static size_t cpart_bytes() {
+    return KSL == 1 ? 0 : (size_t)2 * 4 * NT * 32 * 16;
+  }
+  __host__ __device__ static size_t smem_bytes(int ssl) {
+    return x_bytes(ssl) + red_bytes() + cpart_bytes() + best_bytes();
+  }
+};
+
+template <int WF, int XF, int NT, int D, int KSL>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? TFD_GEMV_MINB_NT1 : 1)
+gemv_kernel(const GemvArgs a) {
+  using L = Layout<WF, XF, NT, KSL>;
+  constexpr int MT = L::MT;
+  constexpr int GR = 16 * MT;  // rows per group
+  using T = WTraits<WF>;
+  constexpr int E = T::E, H = L::H, PL = L::PL, EB = T::ELEM_BYTES;
+  constexpr int MMAJ = E / 4;   // k16 MMAs per step per n-tile
+  constexpr int STEPK = 4 * E;  // k elements per step (4 threads x E)
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int ssl = a.ssl;
+  const int spad = KSL * ssl;
+  uint4* xs = reinterpret_cast<uint4*>(smem);
+  float4* red = reinterpret_cast<float4*>(smem + L::x_bytes(ssl));
+  float4* cpart = reinterpret_cast<float4*>(smem + L::x_bytes(ssl) + L::red_bytes());
+  uint64_t* sbest =
+      reinterpret_cast<uint64_t*>(smem + L::x_bytes(ssl) + L::red_bytes() + L::cpart_bytes());
+  uint64_t* sjoin = sbest + MT * 16;
+  uint32_t* sxmax = reinterpret_cast<uint32_t*>(sjoin + 16 * kWarps);
+  float* sxscale = reinterpret_cast<float*>(sxmax + 16);
+  float2* sms = reinterpret_cast<float2*>(sxscale + 16);   // [MT][16]
+  float2* sjms = sms + MT * 16;                             // [kWarps][16]
+  __shared__ int is_last;
+  // FP8 weights run f16 MMAs: each activation row is scaled by a power of two 2^-e_r into f16 range
+  // (max |x| in [2^14, 2^15)), which keeps every bf16 activation exact down to 2^-32 of the row's
+  // max; the epilogue multiplies by 2^e_r.
+  constexpr bool F16 = WF != TFD_W_BF16;
+  // W8A8: activations quantised per row to E4M3 here, E4M3 x E4M3 MMAs (k = 32)
+  constexpr bool AQ = XF == TFD_X_BF16_E4M3;
+  // block-32 scales (plain or interleaved codes): each step is two 32-wide blocks
+  constexpr bool BLK = WF == TFD_W_FP8_BLOCK32 || WF == TFD_W_FP8_BLOCK32_IL;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int mt = warp % MT, ks = warp / MT;
+  // Split k over a cluster (small vocabularies): block crank of cluster cid takes k-slices
+  // 4 crank .. 4 crank + 3 of every group of the cluster; the leader (crank 0) sums the blocks'
+  // partials in rank order and runs the epilogue.
+  namespace cg = cooperative_groups;
+  const int csplit = KSL == 1 ? 1 : a.csplit;
+  const int crank = csplit > 1 ? (int)cg::this_cluster().block_rank() : 0;
+  const int cid = blockIdx.x / csplit;
+  const int kstep0 = crank * KSL * ssl;  // first step of this block's k range
+  const int64_t K = a.k, N = a.n;
+  const int rows = a.rows;
+
+  // ---- weight stream ----
+  const int64_t g_begin = (int64_t)cid * a.ngroups / a.parts;
+  const int64_t g_end = (int64_t)(cid + 1) * a.ngroups / a.parts;
+  const int s_loc = ks * ssl;              // the k-slice's first step in shared memory
+  const int s_begin = kstep0 + s_loc;      // ... and in the row
+  // The loop runs a multiple of D steps per group so the register ring stays in phase; steps past
+  // the slice's own ssl are empty (no loads, zero weights).
+  const int ssl_loop = (ssl + D - 1) / D * D;
+  const unsigned char* wbase = reinterpret_cast<const unsigned char*>(a.w);
+  const int64_t row_bytes = K * EB;
+  const uint8_t* blk_scales = reinterpret_cast<const uint8_t*>(a.scales);
+  const float* row_scales = reinterpret_cast<const float*>(a.scales);
+  const int64_t kblocks = K >> 5;
+  const bool sc16 = (kblocks & 1) == 0;  // a step's two scale bytes are 2-byte aligned
+
+  // The thread's first element in a step: its 16 contiguous elements, or (block-32 form) its 8
+  // elements of the step's first 32-wide block, the other 8 being 32 further on.
+  const int toff = WF == TFD_W_FP8_BLOCK32 ? 8 * t : t * E;
+  auto steps_below = [&](int64_t lim) -> int {  // steps s < ssl with (s_begin + s) * STEPK < lim
+    int64_t v = lim > 0 ? (lim + STEPK - 1) / STEPK - s_begin : 0;
+    return (int)(v < 0 ? 0 : (v > ssl ? ssl : v));
+  };
+  const int nvalid = steps_below(K - toff);
+  const int nvalid_b = WF == TFD_W_FP8_BLOCK32 ? steps_below(K - 32 - toff) : nvalid;
+
+  // Load state: group, step, row pointer and row validity; addresses advance by a constant.
+  int64_t ld_g = g_begin;
+  int ld_s = 0;
+  const unsigned char* lp = nullptr;
+  const uint8_t* sp = nullptr;
+  bool rv0 = false, rv1 = false, rvb = false;
+  auto set_group = [&]() {
+    const int64_t row = ld_g * GR + mt * 16 + g;
+    const bool in = ld_g < g_end;
+    rv0 = in && row < N;
+    rv1 = in && row + 8 < N;
+    lp = wbase + row * row_bytes + ((int64_t)s_begin * STEPK + toff) * EB;
+    if (BLK) {
+      const int64_t rblk = (ld_g * GR + mt * 16) >> 5;
+      rvb = in && rblk * 32 < N;
+      sp = blk_scales + rblk * kblocks + 2 * (int64_t)s_begin;
+    }
+  };
+  set_group();
+  auto issue = [&](WLoad<WF>& b) {
+    // the usual step: both rows and (block-32 form) both blocks in range, no zero fill
+    const bool full = rv1 && ld_s < (WF == TFD_W_FP8_BLOCK32 ? nvalid_b : nvalid) &&
+                      (!BLK || sc16);
+    if (full) {
+      if (WF == TFD_W_FP8_BLOCK32) {
+        uint2 v = ldg_stream8(lp);
+        b.r[0][0] = v.x; b.r[0][1] = v.y;
+        v = ldg_stream8(lp + 32);
+        b.r[0][2] = v.x; b.r[0][3] = v.y;
+        v = ldg_stream8(lp + 8 * row_bytes);
+        b.r[1][0] = v.x; b.r[1][1] = v.y;
+        v = ldg_stream8(lp + 8 * row_bytes + 32);
+        b.r[1][2] = v.x; b.r[1][3] = v.y;
+        b.scb = __ldg(reinterpret_cast<const uint16_t*>(sp));
+      } else {
+        uint4 v = ldg_stream16(lp);
+        b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
+        v = ldg_stream16(lp + 8 * row_bytes);
+        b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
+        if (WF == TFD_W_FP8_BLOCK32_IL) b.scb = __ldg(reinterpret_cast<const uint16_t*>(sp));
+      }
+      lp += STEPK * EB;
+      sp += 2;
+      if (++ld_s == ssl_loop) { ld_s = 0; ++ld_g; set_group(); }
+      return;
+    }
+#pragma unroll
+    for (int i = 0; i < T::WORDS; ++i) { b.r[0][i] = 0u; b.r[1][i] = 0u; }
+    b.scb = 0u;
+    if (ld_s < nvalid) {
+      if (WF == TFD_W_FP8_BLOCK32) {
+        const bool second = ld_s < nvalid_b;
+        if (rv0) {
+          uint2 v = ldg_stream8(lp);
+          b.r[0][0] = v.x; b.r[0][1] = v.y;
+          if (second) { v = ldg_stream8(lp + 32); b.r[0][2] = v.x; b.r[0][3] = v.y; }
+        }
+        if (rv1) {
+          uint2 v = ldg_stream8(lp + 8 * row_bytes);
+          b.r[1][0] = v.x; b.r[1][1] = v.y;
+          if (second) { v = ldg_stream8(lp + 8 * row_bytes + 32); b.r[1][2] = v.x; b.r[1][3] = v.y; }
+        }
+        if (rvb) {
+          if (sc16) b.scb = __ldg(reinterpret_cast<const uint16_t*>(sp));
+          else b.scb = (uint32_t)__ldg(sp) | ((uint32_t)__ldg(sp + 1) << 8);
+          if (!second) b.scb &= 0xFFu;
+        }
+      } else {
+        if (rv0) {
+          uint4 v = ldg_stream16(lp);
+          b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
+        }
+        if (rv1) {
+          uint4 v = ldg_stream16(lp + 8 * row_bytes);
+          b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
+        }
+        // interleaved block-32 (k % 64 == 0): both blocks of a step are in range together
+        if (WF == TFD_W_FP8_BLOCK32_IL && rvb) b.scb = __ldg(reinterpret_cast<const uint16_t*>(sp));
+      }
+    }
+    lp += STEPK * EB;
+    sp += 2;
+    if (++ld_s == ssl_loop) { ld_s = 0; ++ld_g; set_group(); }
+  };
+
+  // The first D steps of weights are in flight while the activations are staged.
+  WLoad<WF> buf[D];
+#pragma unroll
+  for (int i = 0; i < D; ++i) issue(buf[i]);
+
+  for (int i = tid; i < MT * 16; i += kThreads) sbest[i] = 0ull;
+  if (tid < 16) sxmax[tid] = 0u;
+  __syncthreads();
+  if (F16) {
+    // per-row max |x| over k (non-negative floats order like their bit patterns)
+    const int chunks = (int)((K + 7) / 8);
+    for (int idx = tid; idx < rows * chunks; idx += kThreads) {
+      const int r = idx / chunks;
+      const int k0 = (idx - r * chunks) * 8;
+      float m = 0.0f;
+      if (XF != TFD_X_F32) {
+        uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                                  (int64_t)r * a.ldx + k0);
+        uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(u[i])), fabsf(bf16_hi(u[i]))));
+      } else {
+        const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) +
+                                                          (int64_t)r * a.ldx + k0);
+        float4 u = p[0], w = p[1];
+        m = fmaxf(fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))),
+                  fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
+      }
+      atomicMax(&sxmax[r], __float_as_uint(m));
+    }
+    __syncthreads();
+  }
+  if (tid < 16) {
+    if (AQ) {  // the row's E4M3 scale s = amax / 448 (IEEE division): epilogue factor and divisor
+      const float sx = __fdiv_rn(__uint_as_float(sxmax[tid]), 448.0f);
+      sxscale[tid] = sx;
+      sxmax[tid] = __float_as_uint(sx);
+    } else {
+      int e = 0;
+      const uint32_t ef = (sxmax[tid] >> 23) & 0xFFu;
+      if (F16 && sxmax[tid] != 0u && ef != 0xFFu) {
+        e = (int)ef - 127 - 14;
+        e = e < -110 ? -110 : (e > 110 ? 110 : e);
+      }
+      sxscale[tid] = __uint_as_float((uint32_t)(e + 127) << 23);  // 2^e
+      sxmax[tid] = (uint32_t)(127 - e) << 23;                       // bits of 2^-e
+    }
+  }
+  __syncthreads();
+  // ---- activations -> shared memory, in MMA B-fragment order ----
+  {
+    const int chunks_per_row = spad * STEPK / 8;
+    const int total = 8 * NT * chunks_per_row;
+    for (int idx = tid; idx < total; idx += kThreads) {
+      const int r = idx / chunks_per_row;
+      const int c = idx - r * chunks_per_row;
+      const int k0 = c * 8;  // within the block's k range
+      const int s = k0 / STEPK;
+      const int rem = k0 - s * STEPK;
+      const int64_t kg = (int64_t)kstep0 * STEPK + k0;  // in the whole row
+      // A thread's 16-element chunk is contiguous, except in the block-32 form, where it is 8 elements
+      // of each 32-wide scale block of the step (so every MMA stays inside one block).
+      const int tt = BLK ? (rem & 31) >> 3 : rem / E;
+      const int hf = BLK ? rem >> 5 : (rem - tt * E) >> 3;
+      const int ln = (r & 7) * 4 + tt;
+      const int nt = r >> 3;
+      const bool ok = r < rows && kg < K;
+      const float inv = F16 ? __uint_as_float(sxmax[r]) : 1.0f;
+      if (AQ) {
+        // 8 codes: code = e4m3(fl32(x / s)), s = 0 for a zero row (its codes are zero)
+        uint32_t w0 = 0u, w1 = 0u;
+        if (ok) {
+          const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                                          (int64_t)r * a.ldx + kg);
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+          uint32_t q[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float lo = bf16_lo(u[i]), hi = bf16_hi(u[i]);
+            if (inv > 0.0f) { lo = __fdiv_rn(lo, inv); hi = __fdiv_rn(hi, inv); }
+            q[i] = f32x2_to_e4m3x2(lo, hi);
+          }
+          w0 = q[0] | (q[1] << 16);
+          w1 = q[2] | (q[3] << 16);
+        }
+        reinterpret_cast<uint2*>(xs)[((s * NT + nt) * 32 + ln) * 2 + hf] = make_uint2(w0, w1);
+      } else if (XF == TFD_X_BF16 && !F16) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (ok)
+          v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                              (int64_t)r * a.ldx + kg);
+        xs[((s * NT + nt) * H + hf) * 32 + ln] = v;
+      } else {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = 0.0f;
+        if (ok) {
+          if (XF == TFD_X_BF16) {
+            uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                                      (int64_t)r * a.ldx + kg);
+            uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { f[2 * i] = bf16_lo(u[i]); f[2 * i + 1] = bf16_hi(u[i]); }
+          } else {
+            const float4* p = reinterpret_cast<const float4*>(
+                reinterpret_cast<const float*>(a.x) + (int64_t)r * a.ldx + kg);
+            float4 u = p[0], w = p[1];
+            f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
+            f[4] = w.x; f[5] = w.y; f[6] = w.z; f[7] = w.w;
+          }
+        }
+        uint16_t h[3][8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (PL == 1) h[0][e] = f32_to_f16_bits(f[e] * inv);   // bf16 x, FP8 weights
+          else split3<F16>(f[e] * inv, h[0][e], h[1][e], h[2][e]);
+        }
+#pragma unroll
+        for (int pl = 0; pl < PL; ++pl) {
+          uint4 v;
+          v.x = h[pl][0] | ((uint32_t)h[pl][1] << 16);
+          v.y = h[pl][2] | ((uint32_t)h[pl][3] << 16);
+          v.z = h[pl][4] | ((uint32_t)h[pl][5] << 16);
+          v.w = h[pl][6] | ((uint32_t)h[pl][7] << 16);
+          xs[(((pl * spad + s) * NT + nt) * H + hf) * 32 + ln] = v;
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+
+  // One step: MMA j of the step takes elements [4j, 4j + 4) of each thread's chunk. All activation
+  // fragments of the step are read first; each weight fragment is widened just before its MMAs.
+  // Block-32 form: the step is two 32-wide blocks (MMAs 0-1 and 2-3), each summed on its own and
+  // added to the accumulator times its scale; its activation fragments are read per block, which
+  // keeps fewer registers live.
+  auto compute = [&](const WLoad<WF>& b, int sg, float (&acc)[NT][4]) {
+    if constexpr (AQ) {
+      // MMA j (k = 32) takes codes [8j, 8j + 8) of each thread's 16: one scale block in the block-32
+      // forms. Each MMA starts from zero and is added in fp32 (times its block's scale).
+      uint4 xq[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) xq[nt] = xs[(sg * NT + nt) * 32 + lane];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float sc = BLK ? e8m0_scale((b.scb >> (8 * j)) & 0xFFu) : 1.0f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float c[4];
+          mma_e4m3_16832_z(c, b.r[0][2 * j], b.r[1][2 * j], b.r[0][2 * j + 1], b.r[1][2 * j + 1],
+                           j == 0 ? xq[nt].x : xq[nt].z, j == 0 ? xq[nt].y : xq[nt].w);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[nt][i] = BLK ? fmaf(sc, c[i], acc[nt][i]) : acc[nt][i] + c[i];
+        }
+      }
+    } else if constexpr (BLK) {
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t xq[NT][PL][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int pl = 0; pl < PL; ++pl) {
+            const uint4 v = xs[(((pl * spad + sg) * NT + nt) * H + hb) * 32 + lane];
+            xq[nt][pl][0] = v.x; xq[nt][pl][1] = v.y; xq[nt][pl][2] = v.z; xq[nt][pl][3] = v.w;
+          }
+        float c[NT][4];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          uint32_t A0, A1, A2, A3;
+          e4m3x4_to_f16x2(b.r[0][2 * hb + jj], A0, A2);
+          e4m3x4_to_f16x2(b.r[1][2 * hb + jj], A1, A3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int pl = 0; pl < PL; ++pl) {
+              if (jj == 0 && pl == 0)  // the block's first MMA starts its partial sum
+                mma_f16_16816_z(c[nt], A0, A1, A2, A3, xq[nt][pl][0], xq[nt][pl][1]);
+              else
+                mma_f16_16816(c[nt], A0, A1, A2, A3, xq[nt][pl][2 * jj], xq[nt][pl][2 * jj + 1]);
+            }
+        }
+        const float sc = e8m0_scale((b.scb >> (8 * hb)) & 0xFFu);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[nt][i] = fmaf(sc, c[nt][i], acc[nt][i]);
+      }
+    } else {
+    uint32_t xw[NT][PL][4 * H];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int pl = 0; pl < PL; ++pl)
+#pragma unroll
+        for (int hf = 0; hf < H; ++hf) {
+          uint4 v = xs[(((pl * spad + sg) * NT + nt) * H + hf) * 32 + lane];
+          xw[nt][pl][4 * hf] = v.x; xw[nt][pl][4 * hf + 1] = v.y;
+          xw[nt][pl][4 * hf + 2] = v.z; xw[nt][pl][4 * hf + 3] = v.w;
+        }
+    float c[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[nt][i] = acc[nt][i];
+#pragma unroll
+    for (int j = 0; j < MMAJ; ++j) {
+      uint32_t A0, A1, A2, A3;
+      if (WF == TFD_W_BF16) {
+        A0 = b.r[0][2 * j]; A1 = b.r[1][2 * j]; A2 = b.r[0][2 * j + 1]; A3 = b.r[1][2 * j + 1];
+      } else {
+        e4m3x4_to_f16x2(b.r[0][j], A0, A2);
+        e4m3x4_to_f16x2(b.r[1][j], A1, A3);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int pl = 0; pl < PL; ++pl) {
+          if (F16) mma_f16_16816(c[nt], A0, A1, A2, A3, xw[nt][pl][2 * j], xw[nt][pl][2 * j + 1]);
+          else mma_bf16_16816(c[nt], A0, A1, A2, A3, xw[nt][pl][2 * j], xw[nt][pl][2 * j + 1]);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[nt][i] = c[nt][i];
+    }
+  };
+
+  // Epilogue of one output value: scale, store, rank.
+  // slot = 2 * n-tile + (act & 1); with 4 k-slices a reducer warp handles one n-tile
+  constexpr int BS = KSL == 1 ? 2 * NT : 2;
+  uint64_t best[BS];
+#pragma unroll
+  for (int i = 0; i < BS; ++i) best[i] = 0ull;
+  // online softmax state (max, sum of exp(v - max)) of this thread's outputs, for the confidence
+  float2 ms[BS];
+#pragma unroll
+  for (int i = 0; i < BS; ++i) ms[i] = make_float2(-INFINITY, 0.0f);
+  const bool want_conf = a.topk == 1 && a.top1_conf != nullptr;
+  // Returns the stored value (NaN outside the output).
+  auto epi = [&](int64_t row, int act, float v, int slot) -> float {
+    if (row >= N || act >= rows) return __uint_as_float(0x7FC00000u);
+    if (F16) v *= sxscale[act];
+    if (WF == TFD_W_FP8_ROW) v *= __ldg(row_scales + row);
+    const int64_t yi = (int64_t)act * a.ldy + row;
+    if (a.out_mode == TFD_OUT_F32) {
+      reinterpret_cast<float*>(a.y)[yi] = v;
+    } else if (a.out_mode == TFD_OUT_BF16) {
+      reinterpret_cast<uint16_t*>(a.y)[yi] = f32_to_bf16_bits(v);
+    } else if (a.out_mode == TFD_OUT_ADD_BF16) {
+      uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + yi;
+      *yp = f32_to_bf16_bits(bf16_bits_to_f32(*yp) + v);
+    }
+    if (a.topk == 1) {
+      const int32_t id = a.id_map ? __ldg(a.id_map + row) : (int32_t)row;
+      best[slot] = umax64(best[slot], make_key(v, id));
+      if (want_conf && v > -INFINITY) {  // NaN and -inf add nothing
+        if (v > ms[slot].x) {
+          ms[slot].y = ms[slot].y * expf(ms[slot].x - v) + 1.0f;
+          ms[slot].x = v;
+        } else {
+          ms[slot].y += expf(v - ms[slot].x);
+        }
+      }
+    } else if (a.logits != nullptr && a.logits != a.y) {
+      a.logits[(int64_t)act * a.ld_logits + row] = v;
+    }
+    return v;
+  };
+
+  // Epilogue of one finished MMA tile (rows g, g + 8 of tile `tile` of group gi; activations act0,
+  // act0 + 1), and the tile's sub-group maximum for a later top-k.
+  auto finish_tile = [&](int64_t gi, int tile, int act0, float4 v, int slot0) {
+    const int64_t row_lo = gi * GR + tile * 16 + g;
+    const float o0 = epi(row_lo, act0, v.x, slot0);
+    const float o1 = epi(row_lo, act0 + 1, v.y, slot0 + 1);
+    const float o2 = epi(row_lo + 8, act0, v.z, slot0);
+    const float o3 = epi(row_lo + 8, act0 + 1, v.w, slot0 + 1);
+    if (a.submax != nullptr) {
+      // the 16 rows of this MMA tile are one sub-group: rows g and g + 8 of the eight lanes that
+      // share t
+      uint32_t m0 = max(value_key(o0), value_key(o2));
+      uint32_t m1 = max(value_key(o1), value_key(o3));
+#pragma unroll
+      for (int o = 4; o <= 16; o <<= 1) {
+        m0 = max(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+        m1 = max(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+      }
+      const int64_t sg = gi * MT + tile;
+      const int64_t S = (N + 15) / 16;
+      if (g == 0 && sg < S) {
+        if (act0 < rows) a.submax[(int64_t)act0 * S + sg] = m0;
+        if (act0 + 1 < rows) a.submax[(int64_t)(act0 + 1) * S + sg] = m1;
+      }
+    }
+  };
+
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+  int rb = 0;
+  const int mr = warp & 3, nr = warp >> 2;  // reducer role of warps < 4 * NT
+  for (int64_t gi = g_begin; gi < g_end; ++gi) {
+    for (int s0 = 0; s0 < ssl_loop; s0 += D) {
+#pragma unroll
+      for (int st = 0; st < D; ++st) {
+        // an empty step (past ssl) reads any valid activation slot: its weights are zero
+        compute(buf[st], s_loc + (s0 + st < ssl ? s0 + st : 0), acc);
+        issue(buf[st]);
+      }
+    }
+    if constexpr (KSL == 1) {  // the warp holds whole dot products: epilogue straight away
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        finish_tile(gi, mt, nt * 8 + 2 * t, make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]),
+                    2 * nt);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+      }
+    } else {
+    // k-slice partials -> shared memory; fixed-order sum; epilogue.
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      red[((rb * kWarps + warp) * NT + nt) * 32 + lane] =
+          make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+    }
+    __syncthreads();
+    if (warp < 4 * NT) {
+      // warp index = ks * 4 + mt, so the partials of row tile mr are warps mr, 4+mr, 8+mr, 12+mr.
+      float4 v = red[((rb * kWarps + mr) * NT + nr) * 32 + lane];
+#pragma unroll
+      for (int ksi = 1; ksi < 4; ++ksi) {
+        float4 u = red[((rb * kWarps + ksi * 4 + mr) * NT + nr) * 32 + lane];
+        v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+      }
+      if (csplit == 1) finish_tile(gi, mr, nr * 8 + 2 * t, v, 0);
+      else cpart[(rb * 4 * NT + warp) * 32 + lane] = v;
+    }
+    if (csplit > 1) {
+      cg::this_cluster().sync();  // every block's partial of group gi is in its shared memory
+      if (crank == 0 && warp < 4 * NT) {
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int q = 0; q < csplit; ++q) {  // blocks in rank order
+          const float4 u = cg::this_cluster().map_shared_rank(cpart, q)[(rb * 4 * NT + warp) * 32 + lane];
+          v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+        }
+        finish_tile(gi, mr, nr * 8 + 2 * t, v, 0);
+      }
+      // buffer rb is written again two groups on, after the next barrier: the leader has read it
+    }
+    }
+    rb ^= 1;
+  }
+  if (csplit > 1) {
+    cg::this_cluster().sync();  // the leader has read every block's last partial
+    if (crank != 0) return;
+  }
+
+  if (a.topk != 1) return;
+  // ---- top-1: block best per row, then the last block to finish joins the parts ----
+  if (KSL == 1 || warp < 4 * NT) {
+    // the tile this warp finished, and its n-tiles: (mr, nr) with 4 k-slices, (mt, all) with one
+    const int tile = KSL == 1 ? mt : mr;
+#pragma unroll
+    for (int sl = 0; sl < BS; ++sl) {
+      const int nt = KSL == 1 ? sl >> 1 : nr;
+      const int c = sl & 1;
+      uint64_t key = best[sl];
+      key = umax64(key, shfl_xor_u64(key, 4));
+      key = umax64(key, shfl_xor_u64(key, 8));
+      key = umax64(key, shfl_xor_u64(key, 16));
+      if (g == 0) sbest[tile * 16 + nt * 8 + 2 * t + c] = key;
+      if (want_conf) {
+        float2 q = ms[sl];
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1)
+          q = ms_merge(q, make_float2(__shfl_xor_sync(0xffffffffu, q.x, o),
+                                      __shfl_xor_sync(0xffffffffu, q.y, o)));
+        if (g == 0) sms[tile * 16 + nt * 8 + 2 * t + c] = q;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < kMaxRowsPad) {  // tiles merged in a fixed order
+    uint64_t m = sbest[tid];
+    for (int i = 1; i < MT; ++i) m = umax64(m, sbest[i * 16 + tid]);
+    a.part_keys[(int64_t)cid * kMaxRowsPad + tid] = m;
+    if (want_conf) {
+      float2 q = sms[tid];
+      for (int i = 1; i < MT; ++i) q = ms_merge(q, sms[i * 16 + tid]);
+      a.part_ms[(int64_t)cid * kMaxRowsPad + tid] = q;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = (atomicAdd(a.counter, 1u) == (uint32_t)(a.parts - 1));
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  uint64_t m[kMaxRowsPad];
+#pragma unroll
+  for (int r = 0; r < kMaxRowsPad; ++r) m[r] = 0ull;
+  for (int p = tid; p < a.parts; p += kThreads) {
+#pragma unroll
+    for (int r = 0; r < kMaxRowsPad; ++r)
+      if (r < rows) m[r] = umax64(m[r], __ldcg(a.part_keys + (int64_t)p * kMaxRowsPad + r));
+  }
+#pragma unroll
+  for (int r = 0; r < kMaxRowsPad; ++r) {
+    uint64_t key = m[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) key = umax64(key, shfl_xor_u64(key, o));
+    if (lane == 0) sjoin[warp * kMaxRowsPad + r] = key;
+  }
+  if (want_conf) {
+    // parts are merged in a fixed order: p = tid, tid + 512, ..., then lanes, then warps
+    for (int r = 0; r < rows; ++r) {
+      float2 q = make_float2(-INFINITY, 0.0f);
+      for (int p = tid; p < a.parts; p += kThreads)
+        q = ms_merge(q, __ldcg(a.part_ms + (int64_t)p * kMaxRowsPad + r));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+        q = ms_merge(q, make_float2(__shfl_xor_sync(0xffffffffu, q.x, o),
+                                    __shfl_xor_sync(0xffffffffu, q.y, o)));
+      if (lane == 0) sjms[warp * kMaxRowsPad + r] = q;
+    }
+  }
+  __syncthreads();
+  if (tid < rows) {
+    uint64_t key = 0ull;
+    for (int w = 0; w < kWarps; ++w) key = umax64(key, sjoin[w * kMaxRowsPad + tid]);
+    a.top_vals[tid * a.ldt] = key_value(key);
+    a.top_ids[tid * a.ldt] = key_id(key);
+    if (want_conf) {
+      float2 q = make_float2(-INFINITY, 0.0f);
+      for (int w = 0; w < kWarps; ++w) q = ms_merge(q, sjms[w * kMaxRowsPad + tid]);
+      a.top1_conf[tid] = q.y > 0.0f ? 1.0f / q.y : __uint_as_float(0x7FC00000u);
+    }
+  }
+  if (tid == 0) *a.counter = 0u;  // leave the workspace zeroed
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------------
+
+constexpr size_t kSmemLimit = 232448 - 1024;   // sm_100-class dynamic shared memory, minus slack
+
+template <int WF, int XF, int NT, int KSL = 4>
+size_t gemv_smem(int64_t k, int* ssl_out) {
+  constexpr int E = WTraits<WF>::E;
+  int64_t steps = (k + 4 * E - 1) / (4 * E);
+  int64_t ssl = (steps + KSL - 1) / KSL;
+  if (ssl_out) *ssl_out = (int)ssl;
+  return Layout<WF, XF, NT, KSL>::smem_bytes((int)ssl);
+}
+
+template <int WF, int XF, int NT, int KSL>
+tfd_status gemv_launch_k(GemvArgs a, int parts_req, cudaStream_t stream) {
+  int ssl = 0;
+  size_t smem = gemv_smem<WF, XF, NT, KSL>(a.k, &ssl);
+  if (smem > kSmemLimit) return TFD_ERR_UNSUPPORTED;
+  const int64_t group_rows = 16 * (16 / KSL);
+  a.ngroups = (a.n + group_rows - 1) / group_rows;
+  auto kern = gemv_kernel<WF, XF, NT, gemv_depth<WF, NT, XF>(), KSL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit) !=
+      cudaSuccess)
+    return TFD_ERR_CUDA;
+  int parts = parts_req;
+  int csplit = 1;
+  if (parts <= 0) {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess)
+      return TFD_ERR_CUDA;
+    if (occ < 1) occ = 1;
+    const int64_t slots = (int64_t)tfd_host::sm_count() * occ;
+    if (KSL == 4 && a.ngroups * 2 <= slots) {
+      // Too few groups for the SMs: split k over a cluster of 2, 4 or 8 blocks, keeping at least
+      // a ring's depth of steps per k-slice.
+      constexpr int E = WTraits<WF>::E;
+      constexpr int D = gemv_depth<WF, NT, XF>();
+      const int64_t steps = (a.k + 4 * E - 1) / (4 * E);
+      int64_t c = slots / a.ngroups;
+      if (c > steps / (4 * D)) c = steps / (4 * D);
+      csplit = c >= 8 ? 8 : c >= 4 ? 4 : c >= 2 ? 2 : 1;
+    }
+    int64_t p = slots / csplit;
+    if (p > a.ngroups) p = a.ngroups;
+    if (p > kMaxParts) p = kMaxParts;
+    if (p < 1) p = 1;
+    parts = (int)p;
+  }
+  a.parts = parts;
+  a.csplit = csplit;
+  if (csplit == 1) {
+    a.ssl = ssl;
+    kern<<<parts, kThreads, smem, stream>>>(a);
+    return tfd_host::launch_status();
+  }
+  constexpr int E = WTraits<WF>::E;
+  const int64_t steps = (a.k + 4 * E - 1) / (4 * E);
+  a.ssl = (int)((steps + 4 * csplit - 1) / (4 * csplit));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(parts * csplit));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<WF, XF, NT, KSL>::smem_bytes(a.ssl);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)csplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TFD_ERR_CUDA;
+  return tfd_host::launch_status();
+}
+
+// bf16 weights with a short k (fewer than D steps per k-slice, e.g. the 256-wide second GEMV of
+// the two-stage head) and enough rows for every SM run with one k-slice and 256-row groups.
+template <int WF, int XF, int NT>
+tfd_status gemv_launch_t(GemvArgs a, int parts_req, cudaStream_t stream) {
+  if constexpr (WF == TFD_W_BF16) {
+    constexpr int D = gemv_depth<WF, NT, XF>();
+    const int64_t steps = (a.k + 4 * WTraits<WF>::E - 1) / (4 * WTraits<WF>::E);
+    if ((steps + 3) / 4 < D && (a.n + 255) / 256 >= tfd_host::sm_count())
+      return gemv_launch_k<WF, XF, NT, 1>(a, parts_req, stream);
+  }
+  return gemv_launch_k<WF, XF, NT, 4>(a, parts_req, stream);
+}
+
+template <int WF, int XF>
+tfd_status gemv_launch_nt(GemvArgs a, int parts, cudaStream_t s) {
+  return a.rows <= 8 ? gemv_launch_t<WF, XF, 1>(a, parts, s) : gemv_launch_t<WF, XF, 2>(a, parts, s);
+}
+
+template <int WF>
+tfd_status gemv_launch_x(GemvArgs a, int xfmt, int parts, cudaStream_t s) {
+  if constexpr (WF != TFD_W_BF16) {
+    if (xfmt == TFD_X_BF16_E4M3) return gemv_launch_nt<WF, TFD_X_BF16_E4M3>(a, parts, s);
+  }
+  if (xfmt == TFD_X_BF16_E4M3) return TFD_ERR_INVALID;
+  return xfmt == TFD_X_F32 ? gemv_launch_nt<WF, TFD_X_F32>(a, parts, s)
+                           : gemv_launch_nt<WF, TFD_X_BF16>(a, parts, s);
+}
+
+}  // namespace tfd_gemv
+
+// The launchers each gemv_w*.cu instantiates (and gemv.cu only declares).
+#define TFD_GEMV_EXTERN(WF)                                                                    \
+  extern template tfd_status tfd_gemv::gemv_launch_x<WF>(tfd_gemv::GemvArgs, int, int,          \
+                                                         cudaStream_t);
+#define TFD_GEMV_INSTANTIATE(WF)                                                               \
+  template tfd_status tfd_gemv::gemv_launch_x<WF>(tfd_gemv::GemvArgs, int, int, cudaStream_t);
+

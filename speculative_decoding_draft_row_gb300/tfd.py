@@ -14,7 +14,7 @@ from . import build as _build
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_DATA, ERR_TIMEOUT = range(7)
 W_BF16, W_FP8_ROW, W_FP8_BLOCK32, W_FP8_BLOCK32_IL = 0, 1, 2, 3
-X_BF16, X_F32 = 0, 1
+X_BF16, X_F32, X_BF16_E4M3 = 0, 1, 2
 OUT_NONE, OUT_F32, OUT_BF16, OUT_ADD_BF16 = 0, 1, 2, 3
 MAX_ROWS, MAX_TOPK, MAX_WINDOW = 16, 512, 511
 
@@ -135,14 +135,15 @@ def tfd_head_gemv_max_k(rows, xfmt=X_BF16):
 
 def tfd_head_gemv(w, wfmt, w_scales, x, out_mode=OUT_F32, y=None, topk=0, parts=0, id_map=None,
                   top_vals=None, top_ids=None, ws=None, dev_status=None, n=None, top1_conf=None,
-                  stream=None):
+                  stream=None, act_e4m3=False):
     """Few-row head GEMV with optional output and fused top-k (top-1 optionally with its softmax
-    probability in ``top1_conf`` [rows]). Returns (y, top_vals, top_ids)."""
+    probability in ``top1_conf`` [rows]). ``act_e4m3`` (FP8 weights, bf16 x): quantise the
+    activation rows to E4M3 in the call (W8A8). Returns (y, top_vals, top_ids)."""
     _dev(w, x, y, id_map, ws)
     n = w.shape[0] if n is None else n
     k = w.shape[1]
     rows = x.shape[0]
-    xfmt = X_F32 if x.dtype == torch.float32 else X_BF16
+    xfmt = X_F32 if x.dtype == torch.float32 else (X_BF16_E4M3 if act_e4m3 else X_BF16)
     if y is None and out_mode != OUT_NONE:
         dt = torch.float32 if out_mode == OUT_F32 else torch.bfloat16
         y = torch.empty((rows, n), dtype=dt, device=x.device)

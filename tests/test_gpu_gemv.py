@@ -136,6 +136,46 @@ def test_block32_interleaved_equals_plain_bit_for_bit(n, k, rows, xf32):
     assert_fp32_close(np32(y1), acc, S, "interleaved block-32 logits")
 
 
+W8A8_SHAPES = [(4096, 4096, 1, tfd.W_FP8_ROW), (4096, 4096, 10, tfd.W_FP8_ROW),
+               (1000, 272, 3, tfd.W_FP8_ROW), (4096, 11008, 4, tfd.W_FP8_ROW),
+               (4096, 4096, 5, tfd.W_FP8_BLOCK32), (2080, 1088, 16, tfd.W_FP8_BLOCK32),
+               (4096, 4096, 9, tfd.W_FP8_BLOCK32_IL), (2080, 1088, 1, tfd.W_FP8_BLOCK32_IL)]
+
+
+@pytest.mark.parametrize("n,k,rows,wfmt", W8A8_SHAPES)
+def test_w8a8(n, k, rows, wfmt):
+    """Activations quantised per row to E4M3 in the call (W8A8): fp32-accumulation tolerance
+    against the oracle's exact product of the decoded codes; fused top-8 of its own logits."""
+    need_gpu()
+    base = tfd.W_FP8_BLOCK32 if wfmt == tfd.W_FP8_BLOCK32_IL else wfmt
+    case = make_case(n, k, rows, base, tid=370)
+    w = case["w"] if wfmt != tfd.W_FP8_BLOCK32_IL else tfd.tfd_fp8_block32_relayout(case["w"], True)
+    y, tv, ti = tfd.tfd_head_gemv(w, wfmt, case["scales"], case["x"], tfd.OUT_F32, topk=8,
+                                  act_e4m3=True)
+    torch.cuda.synchronize()
+    acc = og.gemv_acc(case["wo"], case["xo"], base, case["so"], act_fp8=True)
+    S = og.gemv_abs_scale(case["wo"], case["xo"], base, case["so"], act_fp8=True)
+    assert_fp32_close(np32(y), acc, S, "W8A8 logits")
+    ov, oi = oracle_topk(np32(y), 8)
+    assert np.array_equal(ti.cpu().numpy(), oi) and same_bits(np32(tv), ov)
+
+
+def test_w8a8_zero_row_and_refusals():
+    need_gpu()
+    case = make_case(4096, 4096, 3, tfd.W_FP8_ROW, tid=375)
+    x = case["x"].clone()
+    x[1] = 0
+    y, _, _ = tfd.tfd_head_gemv(case["w"], tfd.W_FP8_ROW, case["scales"], x, tfd.OUT_F32,
+                                act_e4m3=True)
+    torch.cuda.synchronize()
+    assert torch.all(y[1] == 0)
+    assert not torch.isnan(y).any()
+    wb = inputs.normal_bf16((64, 256), 0.02, 376).cuda()
+    with pytest.raises(tfd.TfdError):
+        tfd.tfd_head_gemv(wb, tfd.W_BF16, None, inputs.rows(2, 256).cuda(), tfd.OUT_F32,
+                          act_e4m3=True)
+
+
 def test_fused_topk_over_a_long_ragged_vocabulary():
     """270016 logits a row (not a multiple of 8 x 16): the fused top-k from the GEMV's sub-group
     maxima, ragged parts at the end of the row."""

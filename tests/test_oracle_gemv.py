@@ -92,3 +92,23 @@ def test_add_bf16_rounds_once():
 def test_abs_scale_bounds_acc():
     w, x = small(32, 64, 3)
     assert np.all(np.abs(gemv_acc(w, x)) <= gemv_abs_scale(w, x))
+
+
+def test_w8a8_activation_rule_matches_torch_float8_and_closed_forms():
+    """W8A8: each activation row quantised by the weights' row rule; checked against torch's own
+    float8_e4m3fn cast of x / (amax / 448), a one-hot closed form and a zero row."""
+    import torch
+
+    from oracle.gemv import act_e4m3, gemv_acc
+    x = inputs.normal_bf16((6, 4096), 1.5, 980).float().numpy()
+    t = torch.from_numpy(x)
+    s = t.abs().amax(dim=1, keepdim=True) / 448.0
+    ref = (t / s).to(torch.float8_e4m3fn).double() * s.double()
+    assert np.array_equal(act_e4m3(x), ref.numpy())
+    w = inputs.normal_bf16((64, 4096), 0.02, 981).float().numpy()
+    onehot = np.zeros((1, 4096), np.float32)
+    onehot[0, 77] = 3.0
+    got = gemv_acc(w, onehot, W_BF16, None, act_fp8=True)[0]
+    sx = np.float64(np.float32(np.float32(3.0) / np.float32(448.0)))
+    assert np.array_equal(got, w[:, 77].astype(np.float64) * 448.0 * sx)
+    assert np.all(gemv_acc(w, np.zeros((1, 4096), np.float32), W_BF16, None, act_fp8=True) == 0)

@@ -585,6 +585,25 @@ def run_case(args):
         out = torch.empty((PASS_STREAMS, PASS_HEADS * PASS_DIM), dtype=torch.bfloat16,
                           device="cuda")
         fn = lambda: tfd.tfd_window_attn(q, k, v, pos, krd, vrd, PASS_WINDOW, out=out)
+    elif c in ("rows17", "rows24", "rows32"):
+        # a 17-32-row decode window on the full bf16 head: fp32 logits + fused top-1
+        r = int(c[4:])
+        w, _ = inputs.head(tie_frac=0.01)
+        wd = w.cuda()
+        del w
+        xr = inputs.rows(r).cuda()
+        y = torch.empty((r, VOCAB), dtype=torch.float32, device="cuda")
+        tv = torch.empty((r, 1), dtype=torch.float32, device="cuda")
+        ti = torch.empty((r, 1), dtype=torch.int32, device="cuda")
+        ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(r, VOCAB, 1))
+        fn = lambda: tfd.tfd_head_gemv(wd, tfd.W_BF16, None, xr, tfd.OUT_F32, y=y, topk=1,
+                                       top_vals=tv, top_ids=ti, ws=ws)
+        for _ in range(args.warmup):
+            fn()
+        ms = time_graph(fn, args.steps)
+        print(json.dumps({"case": c, "us": round(ms * 1e3, 2),
+                          "gbs": round(bf16_call_bytes(r) / (ms * 1e-3) / 1e9, 1)}), flush=True)
+        return
     elif c in ("rescore", "topk64", "topk512", "twostage"):
         x16 = inputs.rows(16).cuda()
         if c.startswith("topk"):
@@ -676,7 +695,8 @@ def main():
                     help="with --fp8: one row count instead of 1/5/10/15")
     ap.add_argument("--w8a8", action="store_true",
                     help="with --fp8: quantise the activation rows to E4M3 in the call")
-    ap.add_argument("--case", choices=["attn", "rescore", "topk64", "topk512", "twostage"],
+    ap.add_argument("--case", choices=["attn", "rescore", "topk64", "topk512", "twostage",
+                                       "rows17", "rows24", "rows32"],
                     default=None,
                     help="profiling case: one row of the path alone")
     ap.add_argument("--no-extras", action="store_true",

@@ -78,7 +78,10 @@ typedef enum { TFD_X_BF16 = 0, TFD_X_F32 = 1, TFD_X_BF16_E4M3 = 2 } tfd_xfmt;
 typedef enum { TFD_OUT_NONE = 0, TFD_OUT_F32 = 1, TFD_OUT_BF16 = 2, TFD_OUT_ADD_BF16 = 3 } tfd_out;
 
 /* Limits from the pages' statement of the problem. */
-#define TFD_MAX_ROWS 16     /* [TFE] commit "pass kernels and FP8 linears": GEMV for up to 16 rows */
+/* [TFE] commit "pass kernels and FP8 linears": GEMV for up to 16 rows; windows of up to 32 rows
+ * (rows 17-32 take k split over a thread-block cluster where one block's shared memory is too
+ * small for the activation tile; fp32 activations stop at 16 rows). */
+#define TFD_MAX_ROWS 32
 #define TFD_MAX_TOPK 512    /* [TFE] commit "... ocabulary head": cand_k from 1 to 512 */
 #define TFD_MAX_WINDOW 511  /* [TFE] commit "... ocabulary head": window up to 511 (512 keys) */
 
@@ -127,7 +130,8 @@ tfd_status tfd_quant_fp8(const void* w_bf16, int64_t n, int64_t k, int mode, uin
  *   x        device: bf16 or float (xfmt) [rows][ldx], ldx >= k. Float activations are used at
  *            full fp32 precision; TFD_X_BF16_E4M3 (FP8 weights only) quantises bf16 rows to E4M3
  *            first (W8A8, see tfd_xfmt).
- *   rows     1..16.
+ *   rows     1..32 (fp32 activations 1..16). Rows 17-32 go past this page's 16: the subset
+ *            page (#1011) runs decode windows of 17 to 32 rows on wider kernels.
  *   out_mode NONE: no output; F32: y float [rows][ldy] = fl32(acc); BF16: y bf16 = bf16(fl32(acc));
  *            ADD_BF16: y bf16 is read as the residual and overwritten with bf16(res + acc), which
  *            may share memory with nothing else read by the call (in place is allowed).
@@ -146,7 +150,7 @@ tfd_status tfd_quant_fp8(const void* w_bf16, int64_t n, int64_t k, int mode, uin
  *            id_map[i] instead of i (a candidate list or a subset vocabulary, [SUBSET]).
  *   ws       device workspace of tfd_head_gemv_workspace(rows, n, topk, parts) bytes (may be 0).
  *   dev_status device int32 or NULL.
- * Refused: rows outside 1..16; topk > 512 or > n; x aliasing y; NULL or misaligned pointers;
+ * Refused: rows outside 1..32 (1..16 for fp32 activations); topk > 512 or > n; x aliasing y; NULL or misaligned pointers;
  *   rows * k too large for the activation tile (TFD_ERR_UNSUPPORTED, see tfd_head_gemv_max_k).
  */
 size_t tfd_head_gemv_workspace(int rows, int64_t n, int topk, int parts);
@@ -175,7 +179,7 @@ tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scales, int64_t 
  *   the one array: calls whose work overlaps on the GPU (other streams, other threads) race and
  *   must be serialised by the caller. It calls no cudaMalloc, cudaFree or allocating library.
  */
-#define TFD_NOALLOC_SCRATCH_BYTES 524288
+#define TFD_NOALLOC_SCRATCH_BYTES 1048576
 tfd_status tfd_head_gemv_noalloc(const void* w, int wfmt, const void* w_scales, int64_t n,
                                  int64_t k, const void* x, int xfmt, int rows, int64_t ldx,
                                  int out_mode, void* y, int64_t ldy, int topk, int parts,
@@ -207,7 +211,7 @@ tfd_status tfd_topk(const float* logits, int rows, int64_t n, int64_t ld, int k,
  *   ranks last) and sets TFD_ERR_DEVICE_DATA.
  * Args:
  *   w_exact_bf16 device bf16 [vocab][k]; k >= 16, k % 16 == 0.
- *   x_bf16   device bf16 [rows][k]; rows 1..16.
+ *   x_bf16   device bf16 [rows][k]; rows 1..32.
  *   cand     device int32 [rows][cand_k]; cand_k 1..512.
  *   cand_logits device float [rows][cand_k] or NULL.
  *   out_ids  device int32 [rows]; out_vals device float [rows] or NULL.

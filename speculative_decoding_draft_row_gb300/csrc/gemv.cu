@@ -15,20 +15,23 @@ namespace {
 
 using namespace tfd_gemv;
 
-size_t gemv_smem_any(int wfmt, int xfmt, int rows, int64_t k) {
-  const bool two = rows > 8;
-  const bool f32 = xfmt == TFD_X_F32;
-  if (xfmt == TFD_X_BF16_E4M3)  // the same for every FP8 form: 16 codes a lane and step
-    return two ? gemv_smem<TFD_W_FP8_ROW, TFD_X_BF16_E4M3, 2>(k, nullptr)
-               : gemv_smem<TFD_W_FP8_ROW, TFD_X_BF16_E4M3, 1>(k, nullptr);
-#define TFD_SMEM(WF)                                                                    \
-  (two ? (f32 ? gemv_smem<WF, TFD_X_F32, 2>(k, nullptr) : gemv_smem<WF, TFD_X_BF16, 2>(k, nullptr)) \
-       : (f32 ? gemv_smem<WF, TFD_X_F32, 1>(k, nullptr) : gemv_smem<WF, TFD_X_BF16, 1>(k, nullptr)))
-  if (wfmt == TFD_W_FP8_ROW) return TFD_SMEM(TFD_W_FP8_ROW);
-  if (wfmt == TFD_W_FP8_BLOCK32) return TFD_SMEM(TFD_W_FP8_BLOCK32);
-  if (wfmt == TFD_W_FP8_BLOCK32_IL) return TFD_SMEM(TFD_W_FP8_BLOCK32_IL);
-  return TFD_SMEM(TFD_W_BF16);
-#undef TFD_SMEM
+// Whether a call's activation tile fits shared memory (with k split over a cluster if needed).
+bool gemv_fits(int wfmt, int xfmt, int rows, int64_t k) {
+  const int nt = rows <= 8 ? 1 : rows <= 16 ? 2 : 4;
+  if (nt == 4 && xfmt == TFD_X_F32) return false;
+#define TFD_FITS(WF, XF)                                                                       \
+  (nt == 1 ? gemv_min_split<WF, XF, 1, 4>(k) : nt == 2 ? gemv_min_split<WF, XF, 2, 4>(k)         \
+           : gemv_min_split<WF, XF, 4, 4>(k)) > 0
+#define TFD_FITS_X(WF)                                                                         \
+  (xfmt == TFD_X_F32 ? TFD_FITS(WF, TFD_X_F32)                                                 \
+                     : xfmt == TFD_X_BF16_E4M3 ? TFD_FITS(TFD_W_FP8_ROW, TFD_X_BF16_E4M3)        \
+                                               : TFD_FITS(WF, TFD_X_BF16))
+  if (wfmt == TFD_W_FP8_ROW) return TFD_FITS_X(TFD_W_FP8_ROW);
+  if (wfmt == TFD_W_FP8_BLOCK32) return TFD_FITS_X(TFD_W_FP8_BLOCK32);
+  if (wfmt == TFD_W_FP8_BLOCK32_IL) return TFD_FITS_X(TFD_W_FP8_BLOCK32_IL);
+  return TFD_FITS_X(TFD_W_BF16);
+#undef TFD_FITS_X
+#undef TFD_FITS
 }
 
 struct GemvWs {
@@ -46,7 +49,7 @@ struct GemvWs {
 size_t gemv_ws_layout(int rows, int64_t n, int topk, bool logits_in_y, char* base, GemvWs* out) {
   size_t off = 256;
   // top-1: per part a key and an online-softmax pair per row
-  size_t keys = topk == 1 ? tfd_host::round_up((size_t)kMaxParts * kMaxRowsPad * 8, 256) * 2 : 0;
+  size_t keys = topk == 1 ? tfd_host::round_up((size_t)kMaxParts * rows * 8, 256) * 2 : 0;
   size_t lg = (topk > 1 && !logits_in_y) ? tfd_host::round_up((size_t)rows * n * 4, 256) : 0;
   size_t sub = topk > 1 ? tfd_host::round_up((size_t)rows * ((n + 15) / 16) * 4, 256) : 0;
   size_t tk = topk > 1 ? tfd_internal::topk_workspace(rows, n, topk) : 0;
@@ -85,7 +88,7 @@ extern "C" int64_t tfd_head_gemv_max_k(int rows, int xfmt) {
   for (int64_t k = 256; k <= (1 << 20); k += 256) {
     bool ok = true;
     for (int wf = xfmt == TFD_X_BF16_E4M3 ? 1 : 0; wf < 4 && ok; ++wf)
-      ok = gemv_smem_any(wf, xfmt, rows, k) <= kSmemLimit;
+      ok = gemv_fits(wf, xfmt, rows, k);
     if (!ok) break;
     best = k;
   }
@@ -131,7 +134,7 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   GemvWs wl;
   size_t need = gemv_ws_layout(rows, n, topk, logits_in_y, reinterpret_cast<char*>(ws), &wl);
   if (need > 0 && (!ws || ws_bytes < need || !aligned(ws, 16))) return TFD_ERR_WORKSPACE;
-  if (gemv_smem_any(wfmt, xfmt, rows, k) > kSmemLimit) return TFD_ERR_UNSUPPORTED;
+  if (!gemv_fits(wfmt, xfmt, rows, k)) return TFD_ERR_UNSUPPORTED;
 
   GemvArgs a{};
   a.w = w; a.scales = w_scales; a.n = n; a.k = k; a.x = x; a.ldx = ldx; a.rows = rows;

@@ -8,7 +8,7 @@
 // row in parts and a join; the DSpark FP8 head page (#3296), "FP8 draft head": E4M3 codes with
 // E8M0 scales in 32x32 blocks, the drafter's top 64 candidates.
 //
-// Design (GB300, HBM-bound): a 1..16-row GEMV reads every weight byte once, so the kernel is a
+// Design (GB300, HBM-bound): a 1..32-row GEMV reads every weight byte once, so the kernel is a
 // weight stream. Each block is persistent and owns a contiguous range of 64-row groups (one
 // "part" of the vocabulary). Its 16 warps split a group as 4 row tiles x 4 k slices; every warp
 // streams its 16 rows x k-slice straight from HBM into registers with 16-byte (FP8 block form:
@@ -60,9 +60,18 @@ namespace tfd_gemv {
 #ifndef TFD_GEMV_DEPTH_AQ_NT2
 #define TFD_GEMV_DEPTH_AQ_NT2 4
 #endif
+// four n-tiles (17-32 rows)
+#ifndef TFD_GEMV_DEPTH_NT4
+#define TFD_GEMV_DEPTH_NT4 4
+#endif
+#ifndef TFD_GEMV_DEPTH_BLK_NT4
+#define TFD_GEMV_DEPTH_BLK_NT4 2
+#endif
 template <int WF, int NT, int XF = TFD_X_BF16>
 constexpr int gemv_depth() {
-  return (XF == TFD_X_F32 && NT == 2) ? TFD_GEMV_DEPTH_X32_NT2
+  return NT == 4 ? ((WF == TFD_W_FP8_BLOCK32 || WF == TFD_W_FP8_BLOCK32_IL) ? TFD_GEMV_DEPTH_BLK_NT4
+                                                                            : TFD_GEMV_DEPTH_NT4)
+       : (XF == TFD_X_F32 && NT == 2) ? TFD_GEMV_DEPTH_X32_NT2
        : (XF == TFD_X_BF16_E4M3 && NT == 2 && WF == TFD_W_FP8_ROW) ? TFD_GEMV_DEPTH_AQ_NT2
        : WF == TFD_W_BF16 ? (NT == 1 ? TFD_GEMV_DEPTH_NT1 : TFD_GEMV_DEPTH_NT2)
        : WF == TFD_W_FP8_ROW ? (NT == 1 ? TFD_GEMV_DEPTH_FP8_NT1 : TFD_GEMV_DEPTH_FP8_NT2)
@@ -75,7 +84,7 @@ using namespace tfd;
 constexpr int kThreads = 512;
 constexpr int kWarps = 16;
 constexpr int kMaxParts = 1024;
-constexpr int kMaxRowsPad = 16;
+constexpr int kMaxRowsPad = 32;  // activation rows a call takes (four n-tiles of 8)
 
 template <int WF>
 struct WTraits;
@@ -111,13 +120,13 @@ struct GemvArgs {
   float* logits;  // fp32 logits destination for topk > 1 (may equal y), else null
   int64_t ld_logits;
   uint32_t* submax;  // topk > 1: [rows][ceil(n / 16)] value key of each 16-row sub-group's max
-  uint64_t* part_keys;  // [parts][16]
+  uint64_t* part_keys;  // [parts][rows]
   uint32_t* counter;
   float* top_vals;
   int32_t* top_ids;
   int64_t ldt;  // row stride of top_vals / top_ids
   float* top1_conf;  // [rows] softmax probability of the top-1, or null
-  float2* part_ms;   // [parts][16] per part (max, sum of exp(l - max)) for the confidence
+  float2* part_ms;   // [parts][rows] per part (max, sum of exp(l - max)) for the confidence
   int parts;
   int64_t ngroups;
   int ssl;  // steps per k slice
@@ -243,7 +252,8 @@ struct Layout {
   }
   __host__ __device__ static size_t best_bytes() {
     // block best keys, join keys, per-row x max and x scale, block (max, sum) pairs, join pairs
-    return (size_t)MT * 16 * 8 + 16 * kWarps * 8 + 2 * 16 * 4 + MT * 16 * 8 + 16 * kWarps * 8;
+    return (size_t)MT * kMaxRowsPad * 8 + kMaxRowsPad * kWarps * 8 + 2 * kMaxRowsPad * 4 +
+           MT * kMaxRowsPad * 8 + kMaxRowsPad * kWarps * 8;
   }
   // group partials of a block for its cluster leader, double-buffered (4 k-slices only)
   __host__ __device__ static size_t cpart_bytes() {
@@ -272,11 +282,11 @@ gemv_kernel(const GemvArgs a) {
   float4* cpart = reinterpret_cast<float4*>(smem + L::x_bytes(ssl) + L::red_bytes());
   uint64_t* sbest =
       reinterpret_cast<uint64_t*>(smem + L::x_bytes(ssl) + L::red_bytes() + L::cpart_bytes());
-  uint64_t* sjoin = sbest + MT * 16;
-  uint32_t* sxmax = reinterpret_cast<uint32_t*>(sjoin + 16 * kWarps);
-  float* sxscale = reinterpret_cast<float*>(sxmax + 16);
-  float2* sms = reinterpret_cast<float2*>(sxscale + 16);   // [MT][16]
-  float2* sjms = sms + MT * 16;                             // [kWarps][16]
+  uint64_t* sjoin = sbest + MT * kMaxRowsPad;
+  uint32_t* sxmax = reinterpret_cast<uint32_t*>(sjoin + kMaxRowsPad * kWarps);
+  float* sxscale = reinterpret_cast<float*>(sxmax + kMaxRowsPad);
+  float2* sms = reinterpret_cast<float2*>(sxscale + kMaxRowsPad);  // [MT][kMaxRowsPad]
+  float2* sjms = sms + MT * kMaxRowsPad;                             // [kWarps][kMaxRowsPad]
   __shared__ int is_last;
   // FP8 weights run f16 MMAs: each activation row is scaled by a power of two 2^-e_r into f16 range
   // (max |x| in [2^14, 2^15)), which keeps every bf16 activation exact down to 2^-32 of the row's
@@ -415,8 +425,8 @@ gemv_kernel(const GemvArgs a) {
 #pragma unroll
   for (int i = 0; i < D; ++i) issue(buf[i]);
 
-  for (int i = tid; i < MT * 16; i += kThreads) sbest[i] = 0ull;
-  if (tid < 16) sxmax[tid] = 0u;
+  for (int i = tid; i < MT * kMaxRowsPad; i += kThreads) sbest[i] = 0ull;
+  if (tid < kMaxRowsPad) sxmax[tid] = 0u;
   __syncthreads();
   if (F16) {
     // per-row max |x| over k (non-negative floats order like their bit patterns)
@@ -442,7 +452,7 @@ gemv_kernel(const GemvArgs a) {
     }
     __syncthreads();
   }
-  if (tid < 16) {
+  if (tid < kMaxRowsPad) {
     if (AQ) {  // the row's E4M3 scale s = amax / 448 (IEEE division): epilogue factor and divisor
       const float sx = __fdiv_rn(__uint_as_float(sxmax[tid]), 448.0f);
       sxscale[tid] = sx;
@@ -787,26 +797,26 @@ gemv_kernel(const GemvArgs a) {
       key = umax64(key, shfl_xor_u64(key, 4));
       key = umax64(key, shfl_xor_u64(key, 8));
       key = umax64(key, shfl_xor_u64(key, 16));
-      if (g == 0) sbest[tile * 16 + nt * 8 + 2 * t + c] = key;
+      if (g == 0) sbest[tile * kMaxRowsPad + nt * 8 + 2 * t + c] = key;
       if (want_conf) {
         float2 q = ms[sl];
 #pragma unroll
         for (int o = 4; o <= 16; o <<= 1)
           q = ms_merge(q, make_float2(__shfl_xor_sync(0xffffffffu, q.x, o),
                                       __shfl_xor_sync(0xffffffffu, q.y, o)));
-        if (g == 0) sms[tile * 16 + nt * 8 + 2 * t + c] = q;
+        if (g == 0) sms[tile * kMaxRowsPad + nt * 8 + 2 * t + c] = q;
       }
     }
   }
   __syncthreads();
   if (tid < kMaxRowsPad) {  // tiles merged in a fixed order
     uint64_t m = sbest[tid];
-    for (int i = 1; i < MT; ++i) m = umax64(m, sbest[i * 16 + tid]);
-    a.part_keys[(int64_t)cid * kMaxRowsPad + tid] = m;
+    for (int i = 1; i < MT; ++i) m = umax64(m, sbest[i * kMaxRowsPad + tid]);
+    if (tid < rows) a.part_keys[(int64_t)cid * rows + tid] = m;
     if (want_conf) {
       float2 q = sms[tid];
-      for (int i = 1; i < MT; ++i) q = ms_merge(q, sms[i * 16 + tid]);
-      a.part_ms[(int64_t)cid * kMaxRowsPad + tid] = q;
+      for (int i = 1; i < MT; ++i) q = ms_merge(q, sms[i * kMaxRowsPad + tid]);
+      if (tid < rows) a.part_ms[(int64_t)cid * rows + tid] = q;
     }
   }
   __threadfence();
@@ -815,17 +825,11 @@ gemv_kernel(const GemvArgs a) {
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  uint64_t m[kMaxRowsPad];
-#pragma unroll
-  for (int r = 0; r < kMaxRowsPad; ++r) m[r] = 0ull;
-  for (int p = tid; p < a.parts; p += kThreads) {
-#pragma unroll
-    for (int r = 0; r < kMaxRowsPad; ++r)
-      if (r < rows) m[r] = umax64(m[r], __ldcg(a.part_keys + (int64_t)p * kMaxRowsPad + r));
-  }
-#pragma unroll
-  for (int r = 0; r < kMaxRowsPad; ++r) {
-    uint64_t key = m[r];
+#pragma unroll 4
+  for (int r = 0; r < rows; ++r) {
+    uint64_t key = 0ull;
+    for (int p = tid; p < a.parts; p += kThreads)
+      key = umax64(key, __ldcg(a.part_keys + (int64_t)p * rows + r));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) key = umax64(key, shfl_xor_u64(key, o));
     if (lane == 0) sjoin[warp * kMaxRowsPad + r] = key;
@@ -835,7 +839,7 @@ gemv_kernel(const GemvArgs a) {
     for (int r = 0; r < rows; ++r) {
       float2 q = make_float2(-INFINITY, 0.0f);
       for (int p = tid; p < a.parts; p += kThreads)
-        q = ms_merge(q, __ldcg(a.part_ms + (int64_t)p * kMaxRowsPad + r));
+        q = ms_merge(q, __ldcg(a.part_ms + (int64_t)p * rows + r));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1)
         q = ms_merge(q, make_float2(__shfl_xor_sync(0xffffffffu, q.x, o),
@@ -873,11 +877,31 @@ size_t gemv_smem(int64_t k, int* ssl_out) {
   return Layout<WF, XF, NT, KSL>::smem_bytes((int)ssl);
 }
 
+// The smallest cluster split (1, 2, 4 or 8 blocks sharing a group's k range) whose share of the
+// activation tile fits a block's shared memory, or 0 if none does (one k-slice: no split).
+template <int WF, int XF, int NT, int KSL>
+int gemv_min_split(int64_t k) {
+  constexpr int E = WTraits<WF>::E;
+  const int64_t steps = (k + 4 * E - 1) / (4 * E);
+  for (int c = 1; c <= (KSL == 4 ? 8 : 1); c *= 2) {
+    const int64_t ssl = (steps + (int64_t)KSL * c - 1) / ((int64_t)KSL * c);
+    if (Layout<WF, XF, NT, KSL>::smem_bytes((int)ssl) <= kSmemLimit) return c;
+  }
+  return 0;
+}
+
 template <int WF, int XF, int NT, int KSL>
 tfd_status gemv_launch_k(GemvArgs a, int parts_req, cudaStream_t stream) {
   int ssl = 0;
   size_t smem = gemv_smem<WF, XF, NT, KSL>(a.k, &ssl);
-  if (smem > kSmemLimit) return TFD_ERR_UNSUPPORTED;
+  // Up to 16 rows a 4096-wide tile fits one block; 32 rows of it need k split over a cluster.
+  const int cmin = gemv_min_split<WF, XF, NT, KSL>(a.k);
+  if (cmin == 0) return TFD_ERR_UNSUPPORTED;
+  if (cmin > 1) {
+    constexpr int E = WTraits<WF>::E;
+    const int64_t steps = (a.k + 4 * E - 1) / (4 * E);
+    smem = Layout<WF, XF, NT, KSL>::smem_bytes((int)((steps + 4 * cmin - 1) / (4 * cmin)));
+  }
   const int64_t group_rows = 16 * (16 / KSL);
   a.ngroups = (a.n + group_rows - 1) / group_rows;
   auto kern = gemv_kernel<WF, XF, NT, gemv_depth<WF, NT, XF>(), KSL>;
@@ -885,7 +909,7 @@ tfd_status gemv_launch_k(GemvArgs a, int parts_req, cudaStream_t stream) {
       cudaSuccess)
     return TFD_ERR_CUDA;
   int parts = parts_req;
-  int csplit = 1;
+  int csplit = cmin;
   if (parts <= 0) {
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess)
@@ -900,7 +924,8 @@ tfd_status gemv_launch_k(GemvArgs a, int parts_req, cudaStream_t stream) {
       const int64_t steps = (a.k + 4 * E - 1) / (4 * E);
       int64_t c = slots / a.ngroups;
       if (c > steps / (4 * D)) c = steps / (4 * D);
-      csplit = c >= 8 ? 8 : c >= 4 ? 4 : c >= 2 ? 2 : 1;
+      const int want = c >= 8 ? 8 : c >= 4 ? 4 : c >= 2 ? 2 : 1;
+      csplit = want > cmin ? want : cmin;
     }
     int64_t p = slots / csplit;
     if (p > a.ngroups) p = a.ngroups;
@@ -938,7 +963,7 @@ tfd_status gemv_launch_k(GemvArgs a, int parts_req, cudaStream_t stream) {
 // the two-stage head) and enough rows for every SM run with one k-slice and 256-row groups.
 template <int WF, int XF, int NT>
 tfd_status gemv_launch_t(GemvArgs a, int parts_req, cudaStream_t stream) {
-  if constexpr (WF == TFD_W_BF16) {
+  if constexpr (WF == TFD_W_BF16 && NT <= 2) {
     constexpr int D = gemv_depth<WF, NT, XF>();
     const int64_t steps = (a.k + 4 * WTraits<WF>::E - 1) / (4 * WTraits<WF>::E);
     if ((steps + 3) / 4 < D && (a.n + 255) / 256 >= tfd_host::sm_count())
@@ -947,9 +972,14 @@ tfd_status gemv_launch_t(GemvArgs a, int parts_req, cudaStream_t stream) {
   return gemv_launch_k<WF, XF, NT, 4>(a, parts_req, stream);
 }
 
+// Rows 1-8: one n-tile; 9-16: two; 17-32: four (fp32 activations, three operand planes each,
+// stop at 16 rows).
 template <int WF, int XF>
 tfd_status gemv_launch_nt(GemvArgs a, int parts, cudaStream_t s) {
-  return a.rows <= 8 ? gemv_launch_t<WF, XF, 1>(a, parts, s) : gemv_launch_t<WF, XF, 2>(a, parts, s);
+  if (a.rows <= 8) return gemv_launch_t<WF, XF, 1>(a, parts, s);
+  if (a.rows <= 16) return gemv_launch_t<WF, XF, 2>(a, parts, s);
+  if constexpr (XF != TFD_X_F32) return gemv_launch_t<WF, XF, 4>(a, parts, s);
+  return TFD_ERR_UNSUPPORTED;
 }
 
 template <int WF>

@@ -16,7 +16,7 @@ OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_DATA, ERR_
 W_BF16, W_FP8_ROW, W_FP8_BLOCK32, W_FP8_BLOCK32_IL = 0, 1, 2, 3
 X_BF16, X_F32, X_BF16_E4M3 = 0, 1, 2
 OUT_NONE, OUT_F32, OUT_BF16, OUT_ADD_BF16 = 0, 1, 2, 3
-MAX_ROWS, MAX_TOPK, MAX_WINDOW = 16, 512, 511
+MAX_ROWS, MAX_TOPK, MAX_WINDOW = 32, 512, 511
 
 _c = ctypes
 _vp, _i64, _i32, _sz, _f32 = _c.c_void_p, _c.c_int64, _c.c_int, _c.c_size_t, _c.c_float
@@ -165,7 +165,7 @@ def tfd_head_gemv(w, wfmt, w_scales, x, out_mode=OUT_F32, y=None, topk=0, parts=
     return y, top_vals, top_ids
 
 
-NOALLOC_SCRATCH_BYTES = 524288
+NOALLOC_SCRATCH_BYTES = 1048576
 
 
 def tfd_head_gemv_noalloc(w, wfmt, w_scales, x, out_mode=OUT_F32, y=None, topk=0, parts=0,

@@ -39,7 +39,8 @@ def test_workspace_queries():
     assert lib.tfd_head_gemv_workspace(1, 163840, 0, 0) == 0
     assert lib.tfd_head_gemv_workspace(1, 163840, 1, 0) > 0
     assert lib.tfd_head_gemv_workspace(16, 163840, 64, 0) >= 16 * 163840 * 4
-    assert lib.tfd_head_gemv_workspace(17, 163840, 1, 0) == 0          # rows > 16
+    assert lib.tfd_head_gemv_workspace(33, 163840, 1, 0) == 0          # rows > 32
+    assert lib.tfd_head_gemv_workspace(32, 163840, 64, 0) >= 32 * 163840 * 4
     assert lib.tfd_head_gemv_workspace(1, 100, 513, 0) == 0            # topk > 512
     assert lib.tfd_topk_workspace(16, 163840, 512) > 0
     assert lib.tfd_topk_workspace(1, 10, 11) == 0                      # k > n
@@ -48,6 +49,9 @@ def test_workspace_queries():
     assert lib.tfd_head_gemv_max_k(16, tfd.X_BF16) >= 4096
     assert lib.tfd_head_gemv_max_k(4, tfd.X_BF16) >= 11008
     assert lib.tfd_head_gemv_max_k(16, tfd.X_F32) >= 256
+    assert lib.tfd_head_gemv_max_k(32, tfd.X_BF16) >= 4096            # k split over a cluster
+    assert lib.tfd_head_gemv_max_k(32, tfd.X_F32) == 0                # fp32 stops at 16 rows
+    assert lib.tfd_head_gemv_max_k(16, tfd.X_BF16_E4M3) >= 4096
 
 
 FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced by refused calls
@@ -66,7 +70,9 @@ def gemv(**kw):
 
 
 @pytest.mark.parametrize("bad,code", [
-    (dict(rows=0), 1), (dict(rows=17), 1), (dict(k=250), 1), (dict(k=0), 1), (dict(n=0), 1),
+    (dict(rows=0), 1), (dict(rows=33), 1), (dict(k=250), 1), (dict(k=0), 1), (dict(n=0), 1),
+    (dict(wfmt=4), 1), (dict(xfmt=3), 1), (dict(xfmt=2), 1),   # W8A8 needs FP8 weights
+    (dict(rows=17, xfmt=1, ldx=256), 2),                         # fp32 activations: 16 rows
     (dict(w=None), 1), (dict(x=None), 1), (dict(w=FAKE + 8), 1), (dict(ldx=100), 1),
     (dict(wfmt=1), 1), (dict(wfmt=2, ws_=FAKE, n=100), 1), (dict(wfmt=3), 1), (dict(out=4), 1),
     (dict(y=None), 1), (dict(ldy=10), 1), (dict(topk=513), 1), (dict(topk=1), 1),

@@ -50,6 +50,11 @@ SHAPES = [  # (n, k, rows, wfmt, xf32)
     (4177, 4096, 16, tfd.W_BF16, False),
     (2048, 256, 16, tfd.W_BF16, True),        # fp32 activations (low-rank second GEMV)
     (65553, 256, 16, tfd.W_BF16, True),       # short k, many rows: one k-slice, 256-row groups
+    (4096, 4096, 17, tfd.W_BF16, False),      # 17-32 rows: four n-tiles, k split over a cluster
+    (32768, 4096, 32, tfd.W_BF16, False),
+    (4177, 1040, 24, tfd.W_BF16, False),
+    (4096, 4096, 32, tfd.W_FP8_ROW, False),
+    (2048, 4096, 20, tfd.W_FP8_BLOCK32, False),
     (65536, 272, 3, tfd.W_BF16, False),
     (40000, 64, 9, tfd.W_BF16, False),
     (1000, 272, 5, tfd.W_FP8_ROW, False),
@@ -137,6 +142,7 @@ def test_block32_interleaved_equals_plain_bit_for_bit(n, k, rows, xf32):
 
 
 W8A8_SHAPES = [(4096, 4096, 1, tfd.W_FP8_ROW), (4096, 4096, 10, tfd.W_FP8_ROW),
+               (4096, 4096, 32, tfd.W_FP8_ROW), (2080, 4096, 25, tfd.W_FP8_BLOCK32_IL),
                (1000, 272, 3, tfd.W_FP8_ROW), (4096, 11008, 4, tfd.W_FP8_ROW),
                (4096, 4096, 5, tfd.W_FP8_BLOCK32), (2080, 1088, 16, tfd.W_FP8_BLOCK32),
                (4096, 4096, 9, tfd.W_FP8_BLOCK32_IL), (2080, 1088, 1, tfd.W_FP8_BLOCK32_IL)]
@@ -174,6 +180,26 @@ def test_w8a8_zero_row_and_refusals():
     with pytest.raises(tfd.TfdError):
         tfd.tfd_head_gemv(wb, tfd.W_BF16, None, inputs.rows(2, 256).cuda(), tfd.OUT_F32,
                           act_e4m3=True)
+
+
+@pytest.mark.parametrize("wfmt,rows", [(tfd.W_BF16, 32), (tfd.W_FP8_BLOCK32_IL, 19)])
+def test_32_row_window_fused_topk_and_confidence(wfmt, rows):
+    """A 32-row decode window: fused top-64 and top-1 with its confidence, against the oracle."""
+    need_gpu()
+    base = tfd.W_FP8_BLOCK32 if wfmt == tfd.W_FP8_BLOCK32_IL else wfmt
+    case = make_case(8192, 4096, rows, base, tid=380, tie_frac=0.01)
+    w = case["w"] if wfmt != tfd.W_FP8_BLOCK32_IL else tfd.tfd_fp8_block32_relayout(case["w"], True)
+    y, tv, ti = tfd.tfd_head_gemv(w, wfmt, case["scales"], case["x"], tfd.OUT_F32, topk=64)
+    conf = torch.empty(rows, dtype=torch.float32, device="cuda")
+    _, v1, i1 = tfd.tfd_head_gemv(w, wfmt, case["scales"], case["x"], tfd.OUT_NONE, topk=1,
+                                  top1_conf=conf)
+    torch.cuda.synchronize()
+    acc, S = oracle_acc_S(case, base)
+    assert_fp32_close(np32(y), acc, S, "logits")
+    ov, oi = oracle_topk(np32(y), 64)
+    assert np.array_equal(ti.cpu().numpy(), oi) and same_bits(np32(tv), ov)
+    assert np.array_equal(i1.cpu().numpy()[:, 0], oi[:, 0])
+    assert np.allclose(np32(conf), top1_confidence(np32(y)), rtol=1e-4)
 
 
 def test_fused_topk_over_a_long_ragged_vocabulary():

@@ -429,26 +429,47 @@ gemv_kernel(const GemvArgs a) {
   if (tid < kMaxRowsPad) sxmax[tid] = 0u;
   __syncthreads();
   if (F16) {
-    // per-row max |x| over k (non-negative floats order like their bit patterns)
+    // per-row max |x| over k (non-negative floats order like their bit patterns): four loads in
+    // flight per thread, a warp maximum, one shared atomic per warp and row
     const int chunks = (int)((K + 7) / 8);
-    for (int idx = tid; idx < rows * chunks; idx += kThreads) {
-      const int r = idx / chunks;
-      const int k0 = (idx - r * chunks) * 8;
+    for (int r = 0; r < rows; ++r) {
       float m = 0.0f;
-      if (XF != TFD_X_F32) {
-        uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
-                                                  (int64_t)r * a.ldx + k0);
-        uint32_t u[4] = {v.x, v.y, v.z, v.w};
+      for (int c0 = tid; c0 < chunks; c0 += 4 * kThreads) {
+        if (XF != TFD_X_F32) {
+          uint4 v[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(u[i])), fabsf(bf16_hi(u[i]))));
-      } else {
-        const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) +
-                                                          (int64_t)r * a.ldx + k0);
-        float4 u = p[0], w = p[1];
-        m = fmaxf(fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))),
-                  fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
+          for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * kThreads;
+            v[u] = c < chunks ? *reinterpret_cast<const uint4*>(
+                                    reinterpret_cast<const uint16_t*>(a.x) + (int64_t)r * a.ldx + 8 * c)
+                              : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+          }
+        } else {
+          float4 v[4][2];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * kThreads;
+            const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) +
+                                                              (int64_t)r * a.ldx + 8 * c);
+            v[u][0] = c < chunks ? p[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u][1] = c < chunks ? p[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              m = fmaxf(m, fmaxf(fmaxf(fabsf(v[u][h].x), fabsf(v[u][h].y)),
+                                 fmaxf(fabsf(v[u][h].z), fabsf(v[u][h].w))));
+        }
       }
-      atomicMax(&sxmax[r], __float_as_uint(m));
+      m = warp_max(m);
+      if (lane == 0) atomicMax(&sxmax[r], __float_as_uint(m));
     }
     __syncthreads();
   }

@@ -50,8 +50,24 @@ struct RopeTurns {
 
 // Lane l of a warp holds elements 4l..4l+3 of a 128-vector: RMSNorm with gamma, then RoPE with
 // the angle reduced to [-pi, pi) before the fp32 sine and cosine.
-__device__ __forceinline__ void norm_rope(float (&x)[4], const uint16_t* gamma, float eps, int p,
-                                          const RopeTurns& turns) {
+// The sines and cosines of this lane's four pairs at position p (lane l holds pairs
+// 4 (l mod 16) .. + 3), shared by every head at that position.
+__device__ __forceinline__ void rope_sincos(int p, const RopeTurns& turns, float (&sn)[4],
+                                            float (&cs)[4]) {
+  const int lane = threadIdx.x & 31;
+  const float turn_unit = 1.4629180792671596e-9f;  // 2 pi / 2^32
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = 4 * (lane & 15) + j;  // pair index 0..63
+    const uint64_t ph = (uint64_t)(uint32_t)p * turns.t[i];  // mod 2^64: the reduced angle
+    const float red = (float)(int32_t)(ph >> 32) * turn_unit;
+    sincosf(red, &sn[j], &cs[j]);
+  }
+}
+
+// RMSNorm with gamma, then the rotation by the given sines and cosines.
+__device__ __forceinline__ void norm_rope_sc(float (&x)[4], const uint16_t* gamma, float eps,
+                                             const float (&sn)[4], const float (&cs)[4]) {
   const int lane = threadIdx.x & 31;
   float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
   ss = warp_sum(ss);
@@ -65,17 +81,18 @@ __device__ __forceinline__ void norm_rope(float (&x)[4], const uint16_t* gamma, 
 #pragma unroll
   for (int j = 0; j < 4; ++j) other[j] = __shfl_xor_sync(0xffffffffu, x[j], 16);
   const bool first_half = lane < 16;
-  const float turn_unit = 1.4629180792671596e-9f;  // 2 pi / 2^32
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const int i = 4 * (lane & 15) + j;  // pair index 0..63
-    const uint64_t ph = (uint64_t)(uint32_t)p * turns.t[i];  // mod 2^64: the reduced angle
-    const float red = (float)(int32_t)(ph >> 32) * turn_unit;
-    float s, c;
-    sincosf(red, &s, &c);
     // first half holds a = x[i] (partner b = x[i+64]); second half holds b (partner a).
-    x[j] = first_half ? (x[j] * c - other[j] * s) : (other[j] * s + x[j] * c);
+    x[j] = first_half ? (x[j] * cs[j] - other[j] * sn[j]) : (other[j] * sn[j] + x[j] * cs[j]);
   }
+}
+
+__device__ __forceinline__ void norm_rope(float (&x)[4], const uint16_t* gamma, float eps, int p,
+                                          const RopeTurns& turns) {
+  float sn[4], cs[4];
+  rope_sincos(p, turns, sn, cs);
+  norm_rope_sc(x, gamma, eps, sn, cs);
 }
 
 struct AttnPartial {
@@ -284,11 +301,13 @@ absorb_kernel(const uint16_t* __restrict__ k_rows, const uint16_t* __restrict__ 
       vraw[j] = *reinterpret_cast<const uint2*>(v_rows + src + j * kDim);
     }
   }
+  float sn[4], cs[4];
+  rope_sincos(p, turns, sn, cs);  // one position: the same rotation for every head
 #pragma unroll
   for (int j = 0; j < kAbsorbHeads; ++j) {
     if (h0 + j >= heads) break;  // warp-uniform
     float x[4] = {bf16_lo(kraw[j].x), bf16_hi(kraw[j].x), bf16_lo(kraw[j].y), bf16_hi(kraw[j].y)};
-    norm_rope(x, k_gamma, eps, p, turns);
+    norm_rope_sc(x, k_gamma, eps, sn, cs);
     uint2 o;
     o.x = (uint32_t)f32_to_bf16_bits(x[0]) | ((uint32_t)f32_to_bf16_bits(x[1]) << 16);
     o.y = (uint32_t)f32_to_bf16_bits(x[2]) | ((uint32_t)f32_to_bf16_bits(x[3]) << 16);

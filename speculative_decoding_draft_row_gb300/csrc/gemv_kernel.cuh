@@ -48,6 +48,12 @@ namespace tfd_gemv {
 #ifndef TFD_GEMV_DEPTH_BLKIL_NT2
 #define TFD_GEMV_DEPTH_BLKIL_NT2 4
 #endif
+// Bytes of a block's first group fetched into L2 while the activations are staged, and the
+// number of threads that share the request.
+#ifndef TFD_GEMV_PREFETCH
+#define TFD_GEMV_PREFETCH 262144
+#endif
+constexpr int kPrefetchParts = 8;
 // Minimum resident blocks per SM asked of the compiler for one n-tile (2 caps registers at 64).
 #ifndef TFD_GEMV_MINB_NT1
 #define TFD_GEMV_MINB_NT1 1
@@ -424,52 +430,84 @@ gemv_kernel(const GemvArgs a) {
   WLoad<WF> buf[D];
 #pragma unroll
   for (int i = 0; i < D; ++i) issue(buf[i]);
+  // Staging the activations takes longer than the ring's loads (every block reads all rows, which
+  // all blocks want at once); meanwhile the first TFD_GEMV_PREFETCH bytes of the block's first
+  // group are fetched into L2, so the weight stream does not pause.
+  if (csplit == 1 && g_begin < g_end && tid < kPrefetchParts) {
+    const int64_t row0 = g_begin * GR;
+    const int64_t gbytes = (N - row0 < GR ? N - row0 : GR) * row_bytes;
+    const int64_t pbytes = gbytes < (int64_t)TFD_GEMV_PREFETCH ? gbytes : (int64_t)TFD_GEMV_PREFETCH;
+    const int64_t part = (pbytes / kPrefetchParts) & ~(int64_t)15;
+    const int64_t off = tid * part;
+    const int64_t len = tid == kPrefetchParts - 1 ? (pbytes & ~(int64_t)15) - off : part;
+    if (len > 0)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(wbase + row0 * row_bytes + off),
+                   "r"((uint32_t)len)
+                   : "memory");
+  }
 
   for (int i = tid; i < MT * kMaxRowsPad; i += kThreads) sbest[i] = 0ull;
   if (tid < kMaxRowsPad) sxmax[tid] = 0u;
   __syncthreads();
   if (F16) {
-    // per-row max |x| over k (non-negative floats order like their bit patterns): four loads in
-    // flight per thread, a warp maximum, one shared atomic per warp and row
-    const int chunks = (int)((K + 7) / 8);
-    for (int r = 0; r < rows; ++r) {
-      float m = 0.0f;
-      for (int c0 = tid; c0 < chunks; c0 += 4 * kThreads) {
-        if (XF != TFD_X_F32) {
-          uint4 v[4];
+    // per-row max |x| over the whole row (non-negative floats order like their bit patterns): the
+    // chunks of all rows taken together, U loads in flight per thread; a warp whose lanes share a
+    // row takes its maximum and makes one shared atomic, otherwise each lane makes its own
+    constexpr int U = XF == TFD_X_F32 ? 4 : 8;
+    const int chunks = (int)(K / 8);
+    const int total = rows * chunks;
+    for (int base = 0; base < total; base += U * kThreads) {  // the same trip count in every lane
+      float m[U];
+      int rr[U];
+      if (XF != TFD_X_F32) {
+        uint4 v[U];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = c0 + u * kThreads;
-            v[u] = c < chunks ? *reinterpret_cast<const uint4*>(
-                                    reinterpret_cast<const uint16_t*>(a.x) + (int64_t)r * a.ldx + 8 * c)
-                              : make_uint4(0u, 0u, 0u, 0u);
-          }
+        for (int u = 0; u < U; ++u) {
+          const int idx = base + u * kThreads + tid;
+          const bool ok = idx < total;
+          rr[u] = ok ? idx / chunks : 0;
+          v[u] = ok ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                                     (int64_t)rr[u] * a.ldx + 8 * (idx - rr[u] * chunks))
+                    : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        for (int u = 0; u < U; ++u) {
+          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          m[u] = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-          }
-        } else {
-          float4 v[4][2];
+          for (int i = 0; i < 4; ++i) m[u] = fmaxf(m[u], fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        }
+      } else {
+        float4 v[U][2];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = c0 + u * kThreads;
-            const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) +
-                                                              (int64_t)r * a.ldx + 8 * c);
-            v[u][0] = c < chunks ? p[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[u][1] = c < chunks ? p[1] : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
+        for (int u = 0; u < U; ++u) {
+          const int idx = base + u * kThreads + tid;
+          const bool ok = idx < total;
+          rr[u] = ok ? idx / chunks : 0;
+          const float4* p = reinterpret_cast<const float4*>(
+              reinterpret_cast<const float*>(a.x) + (int64_t)rr[u] * a.ldx + 8 * (idx - rr[u] * chunks));
+          v[u][0] = ok ? p[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[u][1] = ok ? p[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < U; ++u) {
+          m[u] = 0.0f;
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              m = fmaxf(m, fmaxf(fmaxf(fabsf(v[u][h].x), fabsf(v[u][h].y)),
-                                 fmaxf(fabsf(v[u][h].z), fabsf(v[u][h].w))));
+          for (int h = 0; h < 2; ++h)
+            m[u] = fmaxf(m[u], fmaxf(fmaxf(fabsf(v[u][h].x), fabsf(v[u][h].y)),
+                                     fmaxf(fabsf(v[u][h].z), fabsf(v[u][h].w))));
         }
       }
-      m = warp_max(m);
-      if (lane == 0) atomicMax(&sxmax[r], __float_as_uint(m));
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r0 = __shfl_sync(0xffffffffu, rr[u], 0);
+        if (__all_sync(0xffffffffu, rr[u] == r0)) {
+          const float mw = warp_max(m[u]);
+          if (lane == 0) atomicMax(&sxmax[r0], __float_as_uint(mw));
+        } else {
+          atomicMax(&sxmax[rr[u]], __float_as_uint(m[u]));
+        }
+      }
     }
     __syncthreads();
   }
@@ -840,20 +878,32 @@ gemv_kernel(const GemvArgs a) {
       if (tid < rows) a.part_ms[(int64_t)cid * rows + tid] = q;
     }
   }
+  if (tid < kMaxRowsPad) sjoin[tid] = 0ull;
   __threadfence();
   __syncthreads();
   if (tid == 0) is_last = (atomicAdd(a.counter, 1u) == (uint32_t)(a.parts - 1));
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-#pragma unroll 4
-  for (int r = 0; r < rows; ++r) {
-    uint64_t key = 0ull;
-    for (int p = tid; p < a.parts; p += kThreads)
-      key = umax64(key, __ldcg(a.part_keys + (int64_t)p * rows + r));
+  {
+    // every part's key of every row in flight at once (8 loads a thread), then a shared maximum
+    // per row (the maximum of keys does not depend on the order)
+    constexpr int U = 8;
+    const int tot = a.parts * rows;  // key i = part i / rows, row i % rows
+    for (int i0 = 0; i0 < tot; i0 += U * kThreads) {
+      uint64_t kk[U];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) key = umax64(key, shfl_xor_u64(key, o));
-    if (lane == 0) sjoin[warp * kMaxRowsPad + r] = key;
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        kk[u] = i < tot ? __ldcg(a.part_keys + i) : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        if (i < tot) atomicMax(reinterpret_cast<unsigned long long*>(&sjoin[i % rows]),
+                               (unsigned long long)kk[u]);
+      }
+    }
   }
   if (want_conf) {
     // parts are merged in a fixed order: p = tid, tid + 512, ..., then lanes, then warps
@@ -870,8 +920,7 @@ gemv_kernel(const GemvArgs a) {
   }
   __syncthreads();
   if (tid < rows) {
-    uint64_t key = 0ull;
-    for (int w = 0; w < kWarps; ++w) key = umax64(key, sjoin[w * kMaxRowsPad + tid]);
+    const uint64_t key = sjoin[tid];
     a.top_vals[tid * a.ldt] = key_value(key);
     a.top_ids[tid * a.ldt] = key_id(key);
     if (want_conf) {

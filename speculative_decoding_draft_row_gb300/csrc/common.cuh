@@ -61,26 +61,39 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
 }
 
 // ---- streaming loads ----------------------------------------------------------------------------
-// Weights are read once per call: bypass L1 and (TFD_L2_PREFETCH=1, the default) ask L2 for
-// 256-byte fetches.
+// Weights are read once per call: bypass L1, ask L2 for 256-byte fetches (TFD_L2_PREFETCH=1, the
+// default) and mark the lines first to be evicted (the policy from l2_stream_policy), so that what
+// a call writes and reads again (logits, sub-group maxima, part keys) stays in L2 meanwhile.
 #ifndef TFD_L2_PREFETCH
 #define TFD_L2_PREFETCH 1
 #endif
-#if TFD_L2_PREFETCH
-#define TFD_LD_STREAM "ld.global.nc.L1::no_allocate.L2::256B"
-#else
-#define TFD_LD_STREAM "ld.global.nc.L1::no_allocate"
+#ifndef TFD_L2_EVICT_FIRST
+#define TFD_L2_EVICT_FIRST 1
 #endif
-__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+#if TFD_L2_PREFETCH
+#define TFD_LD_STREAM "ld.global.nc.L1::no_allocate.L2::cache_hint.L2::256B"
+#else
+#define TFD_LD_STREAM "ld.global.nc.L1::no_allocate.L2::cache_hint"
+#endif
+__device__ __forceinline__ uint64_t l2_stream_policy() {
+  uint64_t pol;
+#if TFD_L2_EVICT_FIRST
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+#else
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+#endif
+  return pol;
+}
+__device__ __forceinline__ uint4 ldg_stream16(const void* p, uint64_t pol) {
   uint4 v;
-  asm volatile(TFD_LD_STREAM ".v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile(TFD_LD_STREAM ".v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "l"(p), "l"(pol));
   return v;
 }
-__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
+__device__ __forceinline__ uint2 ldg_stream8(const void* p, uint64_t pol) {
   uint2 v;
-  asm volatile(TFD_LD_STREAM ".v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  asm volatile(TFD_LD_STREAM ".v2.u32 {%0,%1}, [%2], %3;" : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(pol));
   return v;
 }
 

@@ -360,25 +360,26 @@ gemv_kernel(const GemvArgs a) {
     }
   };
   set_group();
+  const uint64_t wpol = l2_stream_policy();
   auto issue = [&](WLoad<WF>& b) {
     // the usual step: both rows and (block-32 form) both blocks in range, no zero fill
     const bool full = rv1 && ld_s < (WF == TFD_W_FP8_BLOCK32 ? nvalid_b : nvalid) &&
                       (!BLK || sc16);
     if (full) {
       if (WF == TFD_W_FP8_BLOCK32) {
-        uint2 v = ldg_stream8(lp);
+        uint2 v = ldg_stream8(lp, wpol);
         b.r[0][0] = v.x; b.r[0][1] = v.y;
-        v = ldg_stream8(lp + 32);
+        v = ldg_stream8(lp + 32, wpol);
         b.r[0][2] = v.x; b.r[0][3] = v.y;
-        v = ldg_stream8(lp + 8 * row_bytes);
+        v = ldg_stream8(lp + 8 * row_bytes, wpol);
         b.r[1][0] = v.x; b.r[1][1] = v.y;
-        v = ldg_stream8(lp + 8 * row_bytes + 32);
+        v = ldg_stream8(lp + 8 * row_bytes + 32, wpol);
         b.r[1][2] = v.x; b.r[1][3] = v.y;
         b.scb = __ldg(reinterpret_cast<const uint16_t*>(sp));
       } else {
-        uint4 v = ldg_stream16(lp);
+        uint4 v = ldg_stream16(lp, wpol);
         b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
-        v = ldg_stream16(lp + 8 * row_bytes);
+        v = ldg_stream16(lp + 8 * row_bytes, wpol);
         b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
         if (WF == TFD_W_FP8_BLOCK32_IL) b.scb = __ldg(reinterpret_cast<const uint16_t*>(sp));
       }
@@ -394,14 +395,14 @@ gemv_kernel(const GemvArgs a) {
       if (WF == TFD_W_FP8_BLOCK32) {
         const bool second = ld_s < nvalid_b;
         if (rv0) {
-          uint2 v = ldg_stream8(lp);
+          uint2 v = ldg_stream8(lp, wpol);
           b.r[0][0] = v.x; b.r[0][1] = v.y;
-          if (second) { v = ldg_stream8(lp + 32); b.r[0][2] = v.x; b.r[0][3] = v.y; }
+          if (second) { v = ldg_stream8(lp + 32, wpol); b.r[0][2] = v.x; b.r[0][3] = v.y; }
         }
         if (rv1) {
-          uint2 v = ldg_stream8(lp + 8 * row_bytes);
+          uint2 v = ldg_stream8(lp + 8 * row_bytes, wpol);
           b.r[1][0] = v.x; b.r[1][1] = v.y;
-          if (second) { v = ldg_stream8(lp + 8 * row_bytes + 32); b.r[1][2] = v.x; b.r[1][3] = v.y; }
+          if (second) { v = ldg_stream8(lp + 8 * row_bytes + 32, wpol); b.r[1][2] = v.x; b.r[1][3] = v.y; }
         }
         if (rvb) {
           if (sc16) b.scb = __ldg(reinterpret_cast<const uint16_t*>(sp));
@@ -410,11 +411,11 @@ gemv_kernel(const GemvArgs a) {
         }
       } else {
         if (rv0) {
-          uint4 v = ldg_stream16(lp);
+          uint4 v = ldg_stream16(lp, wpol);
           b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
         }
         if (rv1) {
-          uint4 v = ldg_stream16(lp + 8 * row_bytes);
+          uint4 v = ldg_stream16(lp + 8 * row_bytes, wpol);
           b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
         }
         // interleaved block-32 (k % 64 == 0): both blocks of a step are in range together

@@ -49,13 +49,14 @@ rescore_kernel(const uint16_t* __restrict__ w, int64_t vocab, int64_t k,
       set_dev_status(dev_status, TFD_ERR_DEVICE_DATA);
     } else {
       const uint16_t* wr = w + (int64_t)c * k;
+      const uint64_t pol = l2_stream_policy();
       float acc = 0.0f;
       int64_t base = (int64_t)lane * 8;
       for (; base + (kUnroll - 1) * 256 < k; base += kUnroll * 256) {
         uint4 wv[kUnroll], xv[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-          wv[u] = ldg_stream16(wr + base + u * 256);
+          wv[u] = ldg_stream16(wr + base + u * 256, pol);
           xv[u] = __ldg(reinterpret_cast<const uint4*>(xr + base + u * 256));
         }
 #pragma unroll
@@ -70,7 +71,7 @@ rescore_kernel(const uint16_t* __restrict__ w, int64_t vocab, int64_t k,
         }
       }
       for (; base < k; base += 256) {
-        uint4 wv = ldg_stream16(wr + base);
+        uint4 wv = ldg_stream16(wr + base, pol);
         uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + base));
         uint32_t a[4] = {wv.x, wv.y, wv.z, wv.w};
         uint32_t b[4] = {xv.x, xv.y, xv.z, xv.w};

@@ -317,8 +317,20 @@ gemv_kernel(const GemvArgs a) {
   const int rows = a.rows;
 
   // ---- weight stream ----
-  const int64_t g_begin = (int64_t)cid * a.ngroups / a.parts;
-  const int64_t g_end = (int64_t)(cid + 1) * a.ngroups / a.parts;
+  // With 4 k-slices a block owns whole 64-row groups. With one k-slice every warp owns whole dot
+  // products, so the block owns a range of 16-row tiles [t_begin, t_end) instead (finer balance
+  // across blocks: a 256-row group is a large share of a short-k part): warp mt takes tiles
+  // t_begin + mt + 16 j, and "group" j starts at row_off + 256 j.
+  const int64_t ntiles = (N + 15) / 16;
+  const int64_t t_begin = KSL == 1 ? (int64_t)cid * ntiles / a.parts : 0;
+  const int64_t t_end = KSL == 1 ? (int64_t)(cid + 1) * ntiles / a.parts : 0;
+  const int64_t row_off = t_begin * 16;
+  const int64_t g_begin = KSL == 1 ? 0 : (int64_t)cid * a.ngroups / a.parts;
+  const int64_t g_end = KSL == 1 ? (t_end - t_begin + 15) / 16
+                                 : (int64_t)(cid + 1) * a.ngroups / a.parts;
+  auto tile_in = [&](int64_t gi, int tile) {  // the tile is in this block's range
+    return KSL == 1 ? t_begin + 16 * gi + tile < t_end : gi < g_end;
+  };
   const int s_loc = ks * ssl;              // the k-slice's first step in shared memory
   const int s_begin = kstep0 + s_loc;      // ... and in the row
   // The loop runs a multiple of D steps per group so the register ring stays in phase; steps past
@@ -348,13 +360,13 @@ gemv_kernel(const GemvArgs a) {
   const uint8_t* sp = nullptr;
   bool rv0 = false, rv1 = false, rvb = false;
   auto set_group = [&]() {
-    const int64_t row = ld_g * GR + mt * 16 + g;
-    const bool in = ld_g < g_end;
+    const int64_t row = row_off + ld_g * GR + mt * 16 + g;
+    const bool in = tile_in(ld_g, mt);
     rv0 = in && row < N;
     rv1 = in && row + 8 < N;
     lp = wbase + row * row_bytes + ((int64_t)s_begin * STEPK + toff) * EB;
     if (BLK) {
-      const int64_t rblk = (ld_g * GR + mt * 16) >> 5;
+      const int64_t rblk = (row_off + ld_g * GR + mt * 16) >> 5;
       rvb = in && rblk * 32 < N;
       sp = blk_scales + rblk * kblocks + 2 * (int64_t)s_begin;
     }
@@ -435,7 +447,7 @@ gemv_kernel(const GemvArgs a) {
   // all blocks want at once); meanwhile the first TFD_GEMV_PREFETCH bytes of the block's first
   // group are fetched into L2, so the weight stream does not pause.
   if (csplit == 1 && g_begin < g_end && tid < kPrefetchParts) {
-    const int64_t row0 = g_begin * GR;
+    const int64_t row0 = row_off + g_begin * GR;
     const int64_t gbytes = (N - row0 < GR ? N - row0 : GR) * row_bytes;
     const int64_t pbytes = gbytes < (int64_t)TFD_GEMV_PREFETCH ? gbytes : (int64_t)TFD_GEMV_PREFETCH;
     const int64_t part = (pbytes / kPrefetchParts) & ~(int64_t)15;
@@ -755,7 +767,8 @@ gemv_kernel(const GemvArgs a) {
   // Epilogue of one finished MMA tile (rows g, g + 8 of tile `tile` of group gi; activations act0,
   // act0 + 1), and the tile's sub-group maximum for a later top-k.
   auto finish_tile = [&](int64_t gi, int tile, int act0, float4 v, int slot0) {
-    const int64_t row_lo = gi * GR + tile * 16 + g;
+    if (!tile_in(gi, tile)) return;  // warp-uniform: the tile belongs to the next block
+    const int64_t row_lo = row_off + gi * GR + tile * 16 + g;
     const float o0 = epi(row_lo, act0, v.x, slot0);
     const float o1 = epi(row_lo, act0 + 1, v.y, slot0 + 1);
     const float o2 = epi(row_lo + 8, act0, v.z, slot0);
@@ -770,7 +783,7 @@ gemv_kernel(const GemvArgs a) {
         m0 = max(m0, __shfl_xor_sync(0xffffffffu, m0, o));
         m1 = max(m1, __shfl_xor_sync(0xffffffffu, m1, o));
       }
-      const int64_t sg = gi * MT + tile;
+      const int64_t sg = row_off / 16 + gi * MT + tile;
       const int64_t S = (N + 15) / 16;
       if (g == 0 && sg < S) {
         if (act0 < rows) a.submax[(int64_t)act0 * S + sg] = m0;

@@ -15,9 +15,11 @@
 // 8-byte) non-allocating loads kept D steps ahead, and feeds them to warp-level bf16 tensor-core
 // MMAs (m16n8k16, fp32 accumulate) whose other operand is the activation tile held in shared
 // memory in fragment order (conflict-free 16-byte reads). The MMA removes the per-element FMA
-// work that would otherwise cap the CUDA cores at 10-16 rows; FP8 codes are widened to bf16 in
-// registers (exact). The k order inside a dot product is permuted consistently between weights
-// and activations so that each thread's 16 contiguous bytes are one MMA operand chunk.
+// work that would otherwise cap the CUDA cores at 10-16 rows; FP8 codes are widened to f16 in
+// registers (exact), against activations scaled by a power of two into f16 range. The k order
+// inside a dot product is permuted consistently between weights and activations so that each
+// thread's 16 contiguous bytes are one MMA operand chunk. Weight loads carry an L2 evict-first
+// policy, and each block's first group is prefetched into L2 while the activations are staged.
 // Per group, the four k-slice partials are summed in a fixed order in shared memory, so every
 // output's arithmetic is independent of its index and of the part count.
 #pragma once

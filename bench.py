@@ -25,10 +25,27 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 VOCAB, HIDDEN = 163840, 4096
-ROWS = (1, 5, 10, 15)
+ROWS = (1, 5, 10, 15)          # the headline step (the metric's row counts)
+ROWS_SWEEP = (1, 5, 10, 15, 16)  # per-row and FP8 figures: 16 rows is the heaviest case
+L2_BYTES = 129 * 1000 * 1000
+ROTATE_BYTES = 2 * L2_BYTES + 1  # rotated working sets must exceed twice the L2
+ROWS_WINDOW = (17, 24, 32)       # decode windows past 16 rows (bf16 head + top-1)
 METRIC = "head GEMV+top-k achieved HBM GB/s (% of peak) and us/call at 1/5/10/15 rows"
 WORKLOAD = ("full-vocab bf16 head 163840x4096, rows 1/5/10/15, fp32 logits + fused top-1 over "
             "vocabulary parts and a join, 1% planted exact-tie rows")
+
+
+def bench_config(world):
+    """The workload's description, the same on both arms of the bench."""
+    return {"workload": WORKLOAD, "vocab": VOCAB, "hidden": HIDDEN, "rows": list(ROWS),
+            "rows_sweep": list(ROWS_SWEEP), "rows_window": list(ROWS_WINDOW),
+            "l2": "head weights 1.34 GB (FP8 0.67 GB) exceed the 129 MB L2, no flush needed; "
+                  "rows_of_path working sets under twice the L2 are rotated over copies whose "
+                  "total exceeds it",
+            "timing": "value: each step (the four calls at rows 1/5/10/15) replayed from one CUDA "
+                      "graph; per_rows (1/5/10/15/16), per_rows_window (17-32 rows) and "
+                      "fp8_top64 from graphs of 10 calls, us_eager from single eager launches",
+            "parallelism": f"replicas x{world}"}
 
 
 def bf16_call_bytes(rows):
@@ -94,8 +111,22 @@ def oracle_sample_worker(seconds):
                       "threads": int(os.environ.get("OPENBLAS_NUM_THREADS", "0") or 0)}))
 
 
-def run_oracle_sample(seconds):
-    threads = os.cpu_count() or 1
+def cpu_model():
+    """The host CPU's model name from lscpu (None if lscpu is missing)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+    except OSError:
+        return None
+    for line in out.splitlines():
+        if line.lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    return None
+
+
+def run_oracle_sample(seconds, threads=None):
+    """The oracle sample in a fresh process with BLAS limited to ``threads`` (all host cores by
+    default): numpy's matrix product splits the vocabulary rows over the threads."""
+    threads = threads or os.cpu_count() or 1
     env = dict(os.environ, OPENBLAS_NUM_THREADS=str(threads), OMP_NUM_THREADS=str(threads),
                MKL_NUM_THREADS=str(threads))
     out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker",
@@ -108,10 +139,17 @@ def run_oracle_sample(seconds):
 
 
 def cpu_baseline(seconds=12.0):
+    """The oracle timed on the host: all cores (the reported value) and one thread."""
     r = run_oracle_sample(seconds)
+    r1 = run_oracle_sample(seconds / 2, threads=1)
     return {"value": round(r["gbs"], 4), "unit": "GB/s", "cores": r["threads"], "kind": "oracle",
+            "single_thread": {"value": round(r1["gbs"], 4), "unit": "GB/s", "cores": 1,
+                              "seconds": round(r1["seconds"], 1), "calls": r1["calls"]},
+            "nproc": os.cpu_count(), "cpu_model": cpu_model(),
             "sample": f"oracle fp64 GEMV + top-1 on {SAMPLE_ROWS} of the {VOCAB} vocabulary rows "
-                      f"at rows 1/5/10/15, repeated for {r['seconds']:.1f} s ({r['calls']} calls)"}
+                      f"at rows 1/5/10/15, repeated for {r['seconds']:.1f} s ({r['calls']} calls) "
+                      f"with BLAS over all {r['threads']} host threads; single_thread: the same "
+                      f"with one thread"}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -206,34 +244,46 @@ def job_throughput(bytes_per_rank_step, ms_per_step_max, world):
     return bytes_per_rank_step * world / (ms_per_step_max * 1e-3) / 1e9
 
 
+def _rotating(fn):
+    """A list of calls to cycle through: fn itself, or fn's copies when it is a list (each copy
+    on its own buffers, so a working set smaller than L2 is read from HBM)."""
+    return list(fn) if isinstance(fn, (list, tuple)) else [fn]
+
+
 def time_calls(fn, iters, stream):
-    """Mean device time of fn() in ms over iters calls (CUDA events on the launching stream)."""
+    """Mean device time of one call in ms over iters calls, cycling through fn's copies (CUDA
+    events on the launching stream)."""
     import torch
+    fns = _rotating(fn)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     a.record(stream)
-    for _ in range(iters):
-        fn()
+    for i in range(iters):
+        fns[i % len(fns)]()
     b.record(stream)
     b.synchronize()
     return a.elapsed_time(b) / iters
 
 
 def time_graph(fn, iters, per_graph=10):
-    """Mean device time of fn() in ms with the host out of the way: per_graph calls captured in one
-    CUDA graph, replayed until about iters calls ran (CUDA events on the replaying stream)."""
+    """Mean device time of one call in ms with the host out of the way: per_graph calls (at least
+    one round of fn's copies) captured in one CUDA graph, replayed until about iters calls ran
+    (CUDA events on the replaying stream)."""
     import torch
+    fns = _rotating(fn)
+    per_graph = max(per_graph, len(fns))
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        fn()
+        for f in fns:
+            f()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for _ in range(per_graph):
-            fn()
+        for i in range(per_graph):
+            fns[i % len(fns)]()
     reps = max(1, iters // per_graph)
     for _ in range(2):
         g.replay()
@@ -249,6 +299,11 @@ def time_graph(fn, iters, per_graph=10):
     return a.elapsed_time(b) / (reps * per_graph)
 
 
+def copies_for(nbytes):
+    """How many copies of an nbytes working set make the rotated set exceed twice the L2."""
+    return max(1, -(-ROTATE_BYTES // max(1, nbytes)))
+
+
 def run_ours(args):
     import torch
 
@@ -260,12 +315,13 @@ def run_ours(args):
     w, _ = inputs.head(tie_frac=0.01, seed=rank)
     wd = w.cuda()
     del w
-    x_host = inputs.rows(16, seed=rank).pin_memory()
-    xs = {r: x_host[:r].cuda() for r in ROWS}
-    ys = {r: torch.empty((r, VOCAB), dtype=torch.float32, device="cuda") for r in ROWS}
-    tv = {r: torch.empty((r, 1), dtype=torch.float32, device="cuda") for r in ROWS}
-    ti = {r: torch.empty((r, 1), dtype=torch.int32, device="cuda") for r in ROWS}
-    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(16, VOCAB, 1))
+    x_host = inputs.rows(32, seed=rank).pin_memory()
+    all_rows = ROWS_SWEEP + ROWS_WINDOW
+    xs = {r: x_host[:r].cuda() for r in all_rows}
+    ys = {r: torch.empty((r, VOCAB), dtype=torch.float32, device="cuda") for r in all_rows}
+    tv = {r: torch.empty((r, 1), dtype=torch.float32, device="cuda") for r in all_rows}
+    ti = {r: torch.empty((r, 1), dtype=torch.int32, device="cuda") for r in all_rows}
+    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(32, VOCAB, 1))
 
     def call(r, x=None):
         tfd.tfd_head_gemv(wd, tfd.W_BF16, None, xs[r] if x is None else x, tfd.OUT_F32, y=ys[r],
@@ -311,31 +367,32 @@ def run_ours(args):
 
     # eager per-call device times (each call launched on its own, an event pair around it)
     eager_reps = 5
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(eager_reps * len(ROWS) + 1)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(eager_reps * len(all_rows) + 1)]
     evs[0].record(stream)
     i = 0
     for _ in range(eager_reps):
-        for r in ROWS:
+        for r in all_rows:
             call(r)
             i += 1
             evs[i].record(stream)
     evs[-1].synchronize()
-    eager_us = {r: [] for r in ROWS}
+    eager_us = {r: [] for r in all_rows}
     i = 0
     for _ in range(eager_reps):
-        for r in ROWS:
+        for r in all_rows:
             eager_us[r].append(evs[i].elapsed_time(evs[i + 1]) * 1e3)
             i += 1
     # per-call device times with the calls replayed from a CUDA graph (10 calls per graph)
-    graph_us = {r: time_graph(lambda r=r: call(r), 100) * 1e3 for r in ROWS}
+    graph_us = {r: time_graph(lambda r=r: call(r), 100) * 1e3 for r in all_rows}
     pk = peaks()
     peak = pk["hbm_gbs"] if pk else 6800.0
-    per_rows = {}
-    for r in ROWS:
+    per_rows, per_rows_window = {}, {}
+    for r in all_rows:
         us = graph_us[r]
         gbs = bf16_call_bytes(r) / (us * 1e-6) / 1e9
-        per_rows[str(r)] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                            "us_eager": round(statistics.median(eager_us[r]), 2)}
+        (per_rows if r <= 16 else per_rows_window)[str(r)] = {
+            "us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "us_eager": round(statistics.median(eager_us[r]), 2)}
     # the four launches of a step back to back: bytes per launch over the mean launch duration
     achieved = step_bytes / (total_ms / args.steps * 1e-3) / 1e9
 
@@ -376,7 +433,7 @@ def run_ours(args):
         codes, scales = tfd.tfd_quant_fp8(wd, mode)
         ws64 = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(16, VOCAB, 64))
         out = {}
-        for r in ROWS:
+        for r in ROWS_SWEEP:
             v64 = torch.empty((r, 64), dtype=torch.float32, device="cuda")
             i64 = torch.empty((r, 64), dtype=torch.int32, device="cuda")
             f = lambda: tfd.tfd_head_gemv(codes, mode, scales, xs[r], tfd.OUT_NONE, topk=64,
@@ -400,12 +457,9 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) head, N(0,1) rows)",
-        "config": {"workload": WORKLOAD, "vocab": VOCAB, "hidden": HIDDEN, "rows": list(ROWS),
-                   "l2": "weights 1.34 GB exceed the 129 MB L2; no flush needed",
-                   "timing": "each step (the four calls) replayed from one CUDA graph; per_rows from "
-                             "graphs of 10 calls, us_eager from single eager launches",
-                   "parallelism": f"replicas x{world}"},
+        "config": bench_config(world),
         "per_rows": per_rows,
+        "per_rows_window": per_rows_window,
         "fp8_top64": fp8,
         "pass_5x4": draft_pass,
         "rows_of_path": path_rows,
@@ -475,8 +529,11 @@ def measure_pass(wd, stream, reps=20):
 
 
 def measure_rows_of_path(wd, stream, peak):
-    """The other rows of the step, each timed alone (CUDA events, mean over repetitions) and
-    reported as us per call and algorithmic GB/s against the HBM peak."""
+    """The other rows of the step, each timed alone (CUDA-graph replays, mean over repetitions)
+    and reported as us per call and algorithmic GB/s against the HBM peak. A row whose working
+    set is under twice the L2 cycles through copies (new inputs each call) whose total exceeds it,
+    so its bytes come from HBM."""
+    import numpy as np
     import torch
 
     from speculative_decoding_draft_row_gb300 import tfd
@@ -484,20 +541,29 @@ def measure_rows_of_path(wd, stream, peak):
 
     out = {}
 
-    def rec(name, fn, nbytes, reps=20):
+    def rec(name, fn, nbytes, reps=20, working_set=None):
         # device time from graph replays; eager calls add the host's launch overhead
-        for _ in range(3):
-            fn()
-        ms_eager = time_calls(fn, reps, stream)
-        ms = time_graph(fn, reps)
+        fns = _rotating(fn)
+        for f in fns * 2:
+            f()
+        ms_eager = time_calls(fns, max(reps, len(fns)), stream)
+        ms = time_graph(fns, max(reps, 2 * len(fns)))
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"us": round(ms * 1e3, 2), "us_eager": round(ms_eager * 1e3, 2),
                      "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nbytes}
+        if len(fns) > 1:
+            out[name]["rotated"] = {"copies": len(fns), "bytes": len(fns) * working_set}
 
-    # two-stage head, 16 rows: B x, A h, top cand_k of the low-rank logits, exact rescore
-    a, b = inputs.low_rank()
-    ad, bd = a.cuda(), b.cuda()
-    x16 = inputs.rows(16).cuda()
+    # two-stage head, 16 rows: B x, A h, top cand_k of the low-rank logits, exact rescore. Each
+    # copy has its own factors (A + B = 86 MB) and activation rows, so its candidates, and the
+    # exact-head rows the rescore gathers, differ from the other copies'.
+    lr_bytes = 256 * HIDDEN * 2 + VOCAB * 256 * 2
+    ncp = copies_for(lr_bytes)
+    lr = []
+    for c in range(ncp):
+        a, b = inputs.low_rank(seed=c)
+        lr.append((a.cuda(), b.cuda(), inputs.rows(16, seed=c, tensor_id=92).cuda()))
+        del a, b
     h = torch.empty((16, 256), dtype=torch.float32, device="cuda")
     z = torch.empty((16, VOCAB), dtype=torch.float32, device="cuda")
     for ck in (1, 64, 512):
@@ -508,25 +574,59 @@ def measure_rows_of_path(wd, stream, peak):
         oi = torch.empty(16, dtype=torch.int32, device="cuda")
         ov = torch.empty(16, dtype=torch.float32, device="cuda")
 
-        def two_stage():
+        def two_stage(ad, bd, x16):
             tfd.tfd_head_gemv(bd, tfd.W_BF16, None, x16, tfd.OUT_F32, y=h)
             tfd.tfd_head_gemv(ad, tfd.W_BF16, None, h, tfd.OUT_F32, y=z, topk=ck, top_vals=cv,
                               top_ids=ci, ws=tws)
             tfd.tfd_rescore(wd, x16, ci, out_ids=oi, out_vals=ov, ws=rws, want_logits=False)
 
         # what the method must move: B, A, the activations and the gathered exact-head rows
-        nbytes = 256 * HIDDEN * 2 + VOCAB * 256 * 2 + 16 * HIDDEN * 2 + 16 * ck * HIDDEN * 2
-        rec(f"two_stage_cand{ck}", two_stage, nbytes)
-    del ad, bd
-    # window attention of one pass step: 4 streams x 32 heads, window 511 (512 keys)
+        nbytes = lr_bytes + 16 * HIDDEN * 2 + 16 * ck * HIDDEN * 2
+        rec(f"two_stage_cand{ck}", [lambda c=c: two_stage(*lr[c]) for c in range(ncp)], nbytes,
+            working_set=nbytes)
+    del lr
+    # rescore alone: 16 rows x 512 candidate rows of the exact head, new candidates each copy
+    rng = np.random.default_rng([0, 91, 0])
+    nb_rs = 16 * 512 * HIDDEN * 2 + 16 * HIDDEN * 2 + 16 * 512 * 4
+    ncp = copies_for(nb_rs)
+    cands = [torch.from_numpy(rng.integers(0, VOCAB, size=(16, 512)).astype(np.int32)).cuda()
+             for _ in range(ncp)]
+    x16 = inputs.rows(16).cuda()
+    rws = tfd.zeroed_workspace(tfd.tfd_rescore_workspace(16, 512))
+    oi = torch.empty(16, dtype=torch.int32, device="cuda")
+    ov = torch.empty(16, dtype=torch.float32, device="cuda")
+    rec("rescore_16x512", [lambda c=c: tfd.tfd_rescore(wd, x16, cands[c], out_ids=oi, out_vals=ov,
+                                                       ws=rws, want_logits=False)
+                           for c in range(ncp)], nb_rs, working_set=nb_rs)
+    del cands
+    # standalone top-k of 16 x 163840 fp32 logits (10.5 MB a copy)
+    lg_bytes = 16 * VOCAB * 4
+    ncp = copies_for(lg_bytes)
+    logits = [torch.from_numpy(inputs.normal_f32((16, VOCAB), 1.0, 90, seed=c)).cuda()
+              for c in range(ncp)]
+    for kk in (64, 512):
+        tws = tfd.zeroed_workspace(tfd.tfd_topk_workspace(16, VOCAB, kk))
+        cv = torch.empty((16, kk), dtype=torch.float32, device="cuda")
+        ci = torch.empty((16, kk), dtype=torch.int32, device="cuda")
+        rec(f"topk_16x163840_k{kk}",
+            [lambda c=c: tfd.tfd_topk(logits[c], kk, vals=cv, ids=ci, ws=tws) for c in range(ncp)],
+            lg_bytes + 16 * kk * 8, working_set=lg_bytes)
+    del logits
+    # window attention of one pass step: 4 streams x 32 heads, window 511 (512 keys); each copy
+    # its own K/V rings (34.6 MB)
+    ring_bytes = 2 * PASS_STREAMS * PASS_RING * PASS_HEADS * PASS_DIM * 2
+    ncp = copies_for(ring_bytes)
     kr, vr = inputs.rings(PASS_STREAMS, PASS_RING, PASS_HEADS, PASS_DIM)
-    krd, vrd = kr.cuda(), vr.cuda()
+    rings = [(kr.cuda(), vr.cuda()) for _ in range(ncp)]
+    del kr, vr
     q, k, v = (t.cuda() for t in inputs.pass_step_qkv(0))
     pos = torch.full((PASS_STREAMS,), 511, dtype=torch.int32, device="cuda")
     att = torch.empty((PASS_STREAMS, PASS_HEADS * PASS_DIM), dtype=torch.bfloat16, device="cuda")
     rec("window_attn_4x32_w511",
-        lambda: tfd.tfd_window_attn(q, k, v, pos, krd, vrd, PASS_WINDOW, out=att),
-        PASS_STREAMS * PASS_HEADS * (PASS_WINDOW + 1) * PASS_DIM * 2 * 2)
+        [lambda c=c: tfd.tfd_window_attn(q, k, v, pos, rings[c][0], rings[c][1], PASS_WINDOW,
+                                         out=att) for c in range(ncp)],
+        PASS_STREAMS * PASS_HEADS * (PASS_WINDOW + 1) * PASS_DIM * 2 * 2, working_set=ring_bytes)
+    krd, vrd = rings[0]
     # the rest of the head layer: RMSNorm of the hidden rows, SwiGLU, a 128-row prompt-chunk absorb
     hid = torch.from_numpy(inputs.normal_f32((PASS_STREAMS, HIDDEN), 1.0, 61)).to(torch.bfloat16).cuda()
     hout = torch.empty_like(hid)
@@ -543,8 +643,9 @@ def measure_rows_of_path(wd, stream, peak):
     vab = torch.from_numpy(inputs.normal_f32((PASS_STREAMS * nab * PASS_HEADS, PASS_DIM), 1.0, 65)).to(
         torch.bfloat16).cuda().reshape(PASS_STREAMS, nab, PASS_HEADS, PASS_DIM)
     p0 = torch.zeros(PASS_STREAMS, dtype=torch.int32, device="cuda")
-    rec("absorb_4x128rows", lambda: tfd.tfd_absorb(kab, vab, p0, krd, vrd),
-        PASS_STREAMS * nab * PASS_HEADS * PASS_DIM * 2 * 4)
+    rec("absorb_4x128rows",
+        [lambda c=c: tfd.tfd_absorb(kab, vab, p0, rings[c][0], rings[c][1]) for c in range(ncp)],
+        PASS_STREAMS * nab * PASS_HEADS * PASS_DIM * 2 * 4, working_set=ring_bytes)
     # accept of a 5-draft window over 4 streams
     dr = torch.arange(20, dtype=torch.int32, device="cuda").reshape(4, 5)
     na = torch.full((4,), 5, dtype=torch.int32, device="cuda")
@@ -562,7 +663,7 @@ def measure_rows_of_path(wd, stream, peak):
 
 
 def run_fp8_case(args):
-    """A small case for profiling: the FP8 head with fused top-64 (no logits) at rows 1/5/10/15,
+    """A small case for profiling: the FP8 head with fused top-64 (no logits) at rows 1/5/10/15/16,
     warmup + steps calls of each, one JSON line of us per call."""
     import torch
 
@@ -575,9 +676,9 @@ def run_fp8_case(args):
             "block32il": tfd.W_FP8_BLOCK32_IL}[args.fp8]
     w, _ = inputs.head(tie_frac=0.01)
     codes, scales = tfd.tfd_quant_fp8(w.cuda(), mode)
-    row_counts = ROWS if args.rows is None else [args.rows]
-    xs = {r: inputs.rows(16)[:r].cuda() for r in row_counts}
-    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(16, VOCAB, 64))
+    row_counts = ROWS_SWEEP if args.rows is None else [args.rows]
+    xs = {r: inputs.rows(32)[:r].cuda() for r in row_counts}
+    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(32, VOCAB, 64))
     out = {}
     for r in row_counts:
         v = torch.empty((r, 64), dtype=torch.float32, device="cuda")
@@ -693,8 +794,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "vocab": VOCAB, "hidden": HIDDEN,
-                                        "rows": list(ROWS)},
+        "data": "synthetic (seeded N(0,0.02) head, N(0,1) rows)",
+        "config": bench_config(int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": last["threads"],
                          "kind": "oracle",
                          "sample": f"each step: the oracle's fp64 GEMV + top-1 on {SAMPLE_ROWS} of "
@@ -717,8 +818,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", choices=["row", "block32", "block32il"], default=None,
                     help="profiling case: only the FP8 head with fused top-64")
-    ap.add_argument("--rows", type=int, default=None, choices=list(range(1, 17)),
-                    help="with --fp8: one row count instead of 1/5/10/15")
+    ap.add_argument("--rows", type=int, default=None, choices=list(range(1, 33)),
+                    help="with --fp8: one row count instead of 1/5/10/15/16")
     ap.add_argument("--w8a8", action="store_true",
                     help="with --fp8: quantise the activation rows to E4M3 in the call")
     ap.add_argument("--case", choices=["attn", "rescore", "topk64", "topk512", "twostage",

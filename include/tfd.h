@@ -163,9 +163,9 @@ tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scales, int64_t 
 
 /*
  * tfd_head_gemv_noalloc - tfd_head_gemv without a caller workspace, for callers that cannot
- * allocate device memory: code running while a CUDA graph is captured (cudaMalloc is not allowed
- * there), serving loops that keep allocator calls off the hot path because cudaMalloc can block or
- * synchronise the device, and plugins whose host framework owns all device memory.
+ * allocate device memory: serving loops that keep allocator calls off the hot path because
+ * cudaMalloc can block or synchronise the whole device in the middle of a decode round, and plugins
+ * whose host framework owns all device memory and offers them no allocator.
  *   The pages have no counterpart of this entry point; it is an addition of this library.
  *   Same arguments and results as tfd_head_gemv, minus ws/ws_bytes. The scratch is a fixed device
  *   array of TFD_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that loads it until
@@ -173,7 +173,8 @@ tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scales, int64_t 
  *   TFD_ERR_WORKSPACE and enqueues nothing (top-1 calls always fit; a top-k > 1 call fits only when
  *   its fp32 logits and top-k lists do, i.e. for small n).
  *   The first call on a device looks the array's device address up (once per device, with that
- *   device current); make that first call before any stream capture. Each call clears the part of
+ *   device current; a failed lookup is retried by the next call); make that first call before any
+ *   stream capture. Each call clears the part of
  *   the array it uses on `stream` before the GEMV (so a call that then fails an argument check has
  *   already enqueued that clear, which touches only the library's own array). Every call shares
  *   the one array: calls whose work overlaps on the GPU (other streams, other threads) race and

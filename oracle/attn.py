@@ -41,7 +41,7 @@ def rope(v, p, base):
 
 
 def window_attn(q, k_new, v_new, pos, k_ring, v_ring, window, q_gamma=None, k_gamma=None,
-                eps=1e-6, rope_base=10000.0):
+                eps=1e-6, rope_base=10000.0, k_cur=None, terms=None):
     """One decode position per stream.
 
     Args:
@@ -49,22 +49,46 @@ def window_attn(q, k_new, v_new, pos, k_ring, v_ring, window, q_gamma=None, k_ga
       pos: [S] current positions (>= 0).
       k_ring, v_ring: [S][ring][heads][dim] bf16 values (not modified; updated copies returned).
       window: previous keys attended (0..511), ring >= window + 1.
+      k_cur: optional [S][heads][dim] bf16 values taken as the rounded current key instead of
+        the oracle's own rounding of it. Where the exact key lies within fp32 error of a bf16
+        rounding midpoint both neighbours are correct roundings; a check that has accepted the
+        GPU's choice there passes it here, so the output is compared on the same keys.
+      terms: optional dict, filled with the values before the output rounding and the magnitudes
+        that bound an fp32 computation's rounding error (test tolerances are stated against them):
+        ``out_exact`` [S][heads*dim] the attention output before its bf16 rounding;
+        ``k_exact`` [S][heads][dim] the current key before its bf16 rounding;
+        ``k_pair`` [S][heads][dim] the magnitude of each element's rotation pair of the normalised
+        key, sqrt(a_i^2 + a_{i+dim/2}^2) (RoPE preserves it);
+        ``abs_out`` [S][heads*dim] sum_j p_j |v_j|;
+        ``abs_dev`` [S][heads*dim] sum_j p_j |v_j - out|;
+        ``abs_dev_a`` [S][heads*dim] sum_j p_j (A_j + max_i A_i) |v_j - out|, where
+        A_j = sum_e m_e |k_j[e]| / sqrt(dim) with m_e the pair magnitude of the normalised query
+        (A_j bounds |score_j| and scales its rounding error).
     Returns: (out float64 [S][heads*dim] of bf16 values, k_ring', v_ring').
     """
     q = np.asarray(q, dtype=np.float64)
     S, H, D = q.shape
+    half = D // 2
     k_ring = np.array(k_ring, dtype=np.float64, copy=True)
     v_ring = np.array(v_ring, dtype=np.float64, copy=True)
     ring = k_ring.shape[1]
     gq = np.ones(D) if q_gamma is None else np.asarray(q_gamma, dtype=np.float64)
     gk = np.ones(D) if k_gamma is None else np.asarray(k_gamma, dtype=np.float64)
     out = np.empty((S, H * D), dtype=np.float64)
+    if terms is not None:
+        for name, shape in (("out_exact", (S, H * D)), ("k_exact", (S, H, D)),
+                            ("k_pair", (S, H, D)), ("abs_out", (S, H * D)),
+                            ("abs_dev", (S, H * D)), ("abs_dev_a", (S, H * D))):
+            terms[name] = np.zeros(shape, dtype=np.float64)
     for s in range(S):
         p = int(pos[s])
         slot = p % ring
         for h in range(H):
-            qn = rope(rmsnorm(q[s, h], gq, eps), p, rope_base)
-            kn = round_bf16(rope(rmsnorm(k_new[s][h], gk, eps), p, rope_base))
+            qr = rmsnorm(q[s, h], gq, eps)
+            qn = rope(qr, p, rope_base)
+            kr = rmsnorm(k_new[s][h], gk, eps)
+            kx = rope(kr, p, rope_base)
+            kn = round_bf16(kx) if k_cur is None else np.asarray(k_cur[s][h], dtype=np.float64)
             k_ring[s, slot, h] = kn
             v_ring[s, slot, h] = np.asarray(v_new[s][h], dtype=np.float64)
             first = max(0, p - window)
@@ -74,5 +98,17 @@ def window_attn(q, k_new, v_new, pos, k_ring, v_ring, window, q_gamma=None, k_ga
             score = keys @ qn / np.sqrt(D)
             wgt = np.exp(score - score.max())
             wgt /= wgt.sum()
-            out[s, h * D:(h + 1) * D] = round_bf16(wgt @ vals)
+            ox = wgt @ vals
+            out[s, h * D:(h + 1) * D] = round_bf16(ox)
+            if terms is not None:
+                sl = slice(h * D, (h + 1) * D)
+                terms["out_exact"][s, sl] = ox
+                terms["k_exact"][s, h] = kx
+                terms["k_pair"][s, h] = np.tile(np.hypot(kr[:half], kr[half:]), 2)
+                mq = np.tile(np.hypot(qr[:half], qr[half:]), 2)
+                a = np.abs(keys) @ mq / np.sqrt(D)
+                dev = np.abs(vals - ox)
+                terms["abs_out"][s, sl] = wgt @ np.abs(vals)
+                terms["abs_dev"][s, sl] = wgt @ dev
+                terms["abs_dev_a"][s, sl] = (wgt * (a + a.max())) @ dev
     return out, k_ring, v_ring

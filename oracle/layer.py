@@ -23,11 +23,13 @@ from .attn import rmsnorm, rope
 from .numerics import round_bf16
 
 
-def rmsnorm_rows(x, gamma=None, eps=1e-6):
-    """RMSNorm of every row of x [R][H] (bf16 values); returns bf16 values as float64 [R][H]."""
+def rmsnorm_rows(x, gamma=None, eps=1e-6, exact=False):
+    """RMSNorm of every row of x [R][H] (bf16 values); returns bf16 values as float64 [R][H], or
+    with exact=True the values before that rounding."""
     x = np.atleast_2d(np.asarray(x, dtype=np.float64))
     g = np.ones(x.shape[1]) if gamma is None else np.asarray(gamma, dtype=np.float64)
-    return np.stack([round_bf16(rmsnorm(row, g, eps)) for row in x])
+    ex = np.stack([rmsnorm(row, g, eps) for row in x])
+    return ex if exact else round_bf16(ex)
 
 
 def silu(g):
@@ -44,13 +46,17 @@ def swiglu(g, u):
     return round_bf16(s * np.asarray(u, dtype=np.float64))
 
 
-def absorb(k_rows, v_rows, p0, k_ring, v_ring, k_gamma=None, eps=1e-6, rope_base=10000.0):
+def absorb(k_rows, v_rows, p0, k_ring, v_ring, k_gamma=None, eps=1e-6, rope_base=10000.0,
+           terms=None):
     """Write a span of rows into each stream's ring.
 
     Args:
       k_rows, v_rows: [S][n][heads][dim] bf16 values.
       p0: [S] position of each stream's first row (>= 0).
       k_ring, v_ring: [S][ring][heads][dim] (not modified; updated copies returned).
+      terms: optional dict, filled with ``k_exact`` [S][ring][heads][dim], each written key before
+        its bf16 rounding, and ``k_pair``, the magnitude of each element's rotation pair of the
+        normalised key (both NaN at slots the absorb does not write).
     Returns (k_ring', v_ring'). Raises ValueError when n > ring.
     """
     k_rows = np.asarray(k_rows, dtype=np.float64)
@@ -61,11 +67,19 @@ def absorb(k_rows, v_rows, p0, k_ring, v_ring, k_gamma=None, eps=1e-6, rope_base
     if n > ring:
         raise ValueError("an absorb may not write more rows than the ring holds")
     gk = np.ones(D) if k_gamma is None else np.asarray(k_gamma, dtype=np.float64)
+    if terms is not None:
+        terms["k_exact"] = np.full(k_ring.shape, np.nan)
+        terms["k_pair"] = np.full(k_ring.shape, np.nan)
     for s in range(S):
         for i in range(n):
             p = int(p0[s]) + i
             slot = p % ring
             for h in range(H):
-                k_ring[s, slot, h] = round_bf16(rope(rmsnorm(k_rows[s, i, h], gk, eps), p, rope_base))
+                kr = rmsnorm(k_rows[s, i, h], gk, eps)
+                kx = rope(kr, p, rope_base)
+                k_ring[s, slot, h] = round_bf16(kx)
                 v_ring[s, slot, h] = np.asarray(v_rows[s][i][h], dtype=np.float64)
+                if terms is not None:
+                    terms["k_exact"][s, slot, h] = kx
+                    terms["k_pair"][s, slot, h] = np.tile(np.hypot(kr[:D // 2], kr[D // 2:]), 2)
     return k_ring, v_ring

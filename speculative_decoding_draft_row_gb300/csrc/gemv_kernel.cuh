@@ -68,6 +68,12 @@ constexpr int kPrefetchParts = 8;
 #ifndef TFD_GEMV_DEPTH_AQ_NT2
 #define TFD_GEMV_DEPTH_AQ_NT2 4
 #endif
+// CUDA-core form of the bf16 x bf16 step (off by default): the same operands, multiplied with
+// fp32 FMAs instead of tensor-core MMAs. It exists to measure whether the tensor cores pay at this
+// row count; the library is built with it only for that measurement.
+#ifndef TFD_GEMV_FFMA
+#define TFD_GEMV_FFMA 0
+#endif
 // four n-tiles (17-32 rows)
 #ifndef TFD_GEMV_DEPTH_NT4
 #define TFD_GEMV_DEPTH_NT4 4
@@ -631,8 +637,44 @@ gemv_kernel(const GemvArgs a) {
   // Block-32 form: the step is two 32-wide blocks (MMAs 0-1 and 2-3), each summed on its own and
   // added to the accumulator times its scale; its activation fragments are read per block, which
   // keeps fewer registers live.
+  // CUDA-core form: per thread the partial dot products of its two weight rows (g, g + 8) with
+  // every activation row over its k elements, reduced over the four lanes of a row at the end of
+  // the k-slice into the MMA accumulator layout.
+  constexpr bool FFMA = TFD_GEMV_FFMA && WF == TFD_W_BF16 && XF == TFD_X_BF16;
+  float accf[2][FFMA ? 8 * NT : 1];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int c = 0; c < (FFMA ? 8 * NT : 1); ++c) accf[i][c] = 0.0f;
   auto compute = [&](const WLoad<WF>& b, int sg, float (&acc)[NT][4]) {
-    if constexpr (AQ) {
+    if constexpr (FFMA) {
+      float wv[2][8];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          wv[i][2 * e] = bf16_lo(b.r[i][e]);
+          wv[i][2 * e + 1] = bf16_hi(b.r[i][e]);
+        }
+#pragma unroll
+      for (int c = 0; c < 8 * NT; ++c) {
+        if (c < rows) {  // warp-uniform
+          // x[c][the thread's 8 k elements of this step]: the B fragment slot of (c, t)
+          const uint4 v = xs[(sg * NT + (c >> 3)) * 32 + (c & 7) * 4 + t];
+          const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = bf16_lo(xw[e]), x1 = bf16_hi(xw[e]);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              accf[i][c] = fmaf(wv[i][2 * e], x0, accf[i][c]);
+              accf[i][c] = fmaf(wv[i][2 * e + 1], x1, accf[i][c]);
+            }
+          }
+        }
+      }
+      (void)acc;
+    } else if constexpr (AQ) {
       // MMA j (k = 32) takes codes [8j, 8j + 8) of each thread's 16: one scale block in the block-32
       // forms. Each MMA starts from zero and is added in fp32 (times its block's scale).
       uint4 xq[NT];
@@ -809,6 +851,32 @@ gemv_kernel(const GemvArgs a) {
         compute(buf[st], s_loc + (s0 + st < ssl ? s0 + st : 0), acc);
         issue(buf[st]);
       }
+    }
+    if constexpr (FFMA) {
+      // sum over the four lanes of each weight row, then lane t keeps columns 2t, 2t + 1 of each
+      // n-tile, as the MMA accumulator holds them
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int c = 0; c < 8 * NT; ++c) {
+          accf[i][c] += __shfl_xor_sync(0xffffffffu, accf[i][c], 1);
+          accf[i][c] += __shfl_xor_sync(0xffffffffu, accf[i][c], 2);
+        }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = q >> 1, h = q & 1;
+          float v = accf[i][nt * 8 + h];
+#pragma unroll
+          for (int tt = 1; tt < 4; ++tt)
+            if (t == tt) v = accf[i][nt * 8 + 2 * tt + h];
+          acc[nt][q] = v;
+        }
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int c = 0; c < 8 * NT; ++c) accf[i][c] = 0.0f;
     }
     if constexpr (KSL == 1) {  // the warp holds whole dot products: epilogue straight away
 #pragma unroll

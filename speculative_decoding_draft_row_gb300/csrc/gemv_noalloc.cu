@@ -1,11 +1,10 @@
 // gemv_noalloc.cu - tfd_head_gemv for callers that cannot allocate device memory.
 //
-// Some callers have no way to obtain device scratch: code that runs while a CUDA graph is being
-// captured (where cudaMalloc is not allowed), serving loops that forbid allocator calls on the hot
-// path because cudaMalloc can block or synchronise the device, and plugins whose host framework
-// owns all device memory and offers no allocator to them. This entry point runs the same head
-// GEMV as tfd_head_gemv, but its scratch is a fixed file-scope device array, so the caller only
-// passes inputs and outputs.
+// Some callers have no way to obtain device scratch: serving loops that forbid allocator calls on
+// the hot path (cudaMalloc can block, or synchronise the whole device, in the middle of a decode
+// round), and plugins whose host framework owns all device memory and offers them no allocator.
+// This entry point runs the same head GEMV as tfd_head_gemv, but its scratch is a fixed
+// file-scope device array, so the caller only passes inputs and outputs.
 #include <mutex>
 
 #include "common.cuh"
@@ -19,22 +18,25 @@ constexpr int kMaxDevices = 64;
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[TFD_NOALLOC_SCRATCH_BYTES];
 
-std::once_flag g_once[kMaxDevices];
-void* g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+std::mutex g_lock[kMaxDevices];
+void* g_scratch_ptr[kMaxDevices];  // set only after a successful lookup
 
 // Device address of the scratch on the current device, looked up once per device (with that
-// device current, as it is during the call that does the lookup).
+// device current, as it is during the call that does the lookup). A failed lookup is not cached:
+// its error is cleared from the runtime's last-error slot and the next call tries again.
 tfd_status scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return TFD_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return TFD_ERR_UNSUPPORTED;
-  std::call_once(g_once[dev], [dev] {
+  std::lock_guard<std::mutex> guard(g_lock[dev]);
+  if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return TFD_ERR_CUDA;
+    }
     g_scratch_ptr[dev] = p;
-  });
-  if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return TFD_ERR_CUDA;
+  }
   *out = g_scratch_ptr[dev];
   return TFD_OK;
 }

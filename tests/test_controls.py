@@ -5,10 +5,13 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import assert_bf16_close, need_gpu, np32
+from helpers import (NORM_REL, assert_bf16_rounding, check_window_attn, gemv_bf16_err, need_gpu,
+                     np32)
 from oracle import attn as oattn
+from oracle import gemv as og
 from oracle import numerics
 from oracle.accept import accept
+from oracle.layer import rmsnorm_rows
 from oracle.quant import quant_fp8_block32, quant_fp8_row
 from oracle.topk import order, topk
 from synth import inputs
@@ -74,6 +77,29 @@ def rope_interleaved(v, p, base):
     return out
 
 
+def trunc_bf16(x):
+    """bf16 by truncation toward zero instead of round-to-nearest-even."""
+    x = np.asarray(x, dtype=np.float64)
+    out = x.copy()
+    fin = np.isfinite(x)
+    _, e = np.frexp(x[fin])
+    q = np.maximum(e - 8, -133)
+    out[fin] = np.ldexp(np.trunc(np.ldexp(x[fin], -q)), q)
+    return out
+
+
+def round_half_away_bf16(x):
+    """bf16 rounding to nearest with ties away from zero instead of to even."""
+    x = np.asarray(x, dtype=np.float64)
+    out = x.copy()
+    fin = np.isfinite(x)
+    _, e = np.frexp(x[fin])
+    q = np.maximum(e - 8, -133)
+    m = np.ldexp(x[fin], -q)
+    out[fin] = np.ldexp(np.sign(m) * np.floor(np.abs(m) + 0.5), q)
+    return out
+
+
 def accept_count_all_equal(drafts, n_asked, draws):
     """Counts every equal position instead of the equal prefix."""
     d, w = np.asarray(drafts), np.asarray(draws)
@@ -129,6 +155,24 @@ def test_control_accept_prefix_rule_is_caught():
     assert accept_count_all_equal(drafts, [5], draws)[0] != 2
 
 
+def test_control_bf16_rounding_check_catches_truncation_and_ties_away():
+    """The bf16 check holds values to round-to-nearest-even: fp32 results (the exact value plus an
+    fp32-sized error) rounded by the method pass; the same results truncated, or with ties rounded
+    away from zero, fail."""
+    rng = np.random.default_rng([0, 803, 0])
+    exact = rng.normal(0.0, 1.0, 20000) * np.exp2(rng.integers(-20, 20, 20000))
+    err = 1e-6 * np.abs(exact)
+    gpu_like = numerics.round_bf16(numerics.fl32(exact).astype(np.float64))
+    assert_bf16_rounding(gpu_like, exact, err)
+    with pytest.raises(AssertionError):
+        assert_bf16_rounding(trunc_bf16(exact), exact, err)
+    # exact ties: bf16 midpoints, which the even rule and the away rule round differently
+    mids = (np.arange(1, 4000, 2) + 256.0) * 2.0 ** -9
+    assert_bf16_rounding(numerics.round_bf16(mids), mids, 0.0)
+    with pytest.raises(AssertionError):
+        assert_bf16_rounding(round_half_away_bf16(mids), mids, 0.0)
+
+
 # ---- GPU controls: the same mutants disagree with the CUDA path ----------------------------------
 
 @pytest.mark.gpu
@@ -165,13 +209,55 @@ def test_gpu_control_rope_pairing(monkeypatch):
     q, k, v = (inputs.normal_bf16((S, H, D), 1.0, 820 + i) for i in range(3))
     kr = inputs.normal_bf16((S * ring, H, D), 1.0, 823).reshape(S, ring, H, D)
     vr = inputs.normal_bf16((S * ring, H, D), 1.0, 824).reshape(S, ring, H, D)
+    kd, vd = kr.clone().cuda(), vr.clone().cuda()
     out = tfd.tfd_window_attn(q.cuda(), k.cuda(), v.cuda(), torch.tensor([9], dtype=torch.int32,
-                              device="cuda"), kr.clone().cuda(), vr.clone().cuda(), 9)
+                              device="cuda"), kd, vd, 9)
     torch.cuda.synchronize()
     f = lambda t: t.float().numpy()
-    good, _, _ = oattn.window_attn(f(q), f(k), f(v), [9], f(kr), f(vr), 9)
-    assert_bf16_close(np32(out), good)
+    args = (f(q), f(k), f(v), [9], f(kr), f(vr), 9)
+    check_window_attn(np32(out), np32(kd), np32(vd), *args)
     monkeypatch.setattr(oattn, "rope", rope_interleaved)
-    bad, _, _ = oattn.window_attn(f(q), f(k), f(v), [9], f(kr), f(vr), 9)
     with pytest.raises(AssertionError):
-        assert_bf16_close(np32(out), bad)
+        check_window_attn(np32(out), np32(kd), np32(vd), *args)
+
+
+@pytest.mark.gpu
+def test_gpu_control_bf16_truncation_is_caught():
+    """An oracle that truncated to bf16 (instead of rounding to nearest even) fails against the
+    GPU's bf16 outputs: GEMV out BF16 and ADD_BF16, RMSNorm, and the attention's output and ring
+    keys."""
+    need_gpu()
+    from speculative_decoding_draft_row_gb300 import tfd
+    w = inputs.normal_bf16((4096, 4096), 0.02, 830)
+    x = inputs.normal_bf16((4, 4096), 1.0, 831)
+    res = inputs.normal_bf16((4, 4096), 1.0, 832)
+    y, _, _ = tfd.tfd_head_gemv(w.cuda(), tfd.W_BF16, None, x.cuda(), tfd.OUT_BF16)
+    ya = res.clone().cuda()
+    tfd.tfd_head_gemv(w.cuda(), tfd.W_BF16, None, x.cuda(), tfd.OUT_ADD_BF16, y=ya)
+    hid = inputs.normal_bf16((4, 4096), 3.0, 833)
+    hn = tfd.tfd_rmsnorm(hid.cuda(), None, 1e-6)
+    torch.cuda.synchronize()
+    acc = og.gemv_acc(w.float().numpy(), x.float().numpy())
+    S = og.gemv_abs_scale(w.float().numpy(), x.float().numpy())
+    ex_add = res.float().numpy().astype(np.float64) + acc
+    ex_norm = rmsnorm_rows(hid.float().numpy(), None, 1e-6, exact=True)
+    checks = [(np32(y), acc, gemv_bf16_err(S)), (np32(ya), ex_add, gemv_bf16_err(S, ex_add)),
+              (np32(hn), ex_norm, NORM_REL * np.abs(ex_norm))]
+    for got, ex, err in checks:
+        assert_bf16_rounding(got, ex, err)
+        with pytest.raises(AssertionError):
+            assert_bf16_rounding(got, ex, err, rnd=trunc_bf16)
+    S_, H, D, ring = 4, 32, 128, 528
+    q, k, v = (inputs.normal_bf16((S_, H, D), 1.0, 840 + i) for i in range(3))
+    kr = inputs.normal_bf16((S_ * ring, H, D), 1.0, 843).reshape(S_, ring, H, D)
+    vr = inputs.normal_bf16((S_ * ring, H, D), 1.0, 844).reshape(S_, ring, H, D)
+    pos = [511, 512, 513, 515]
+    kd, vd = kr.clone().cuda(), vr.clone().cuda()
+    out = tfd.tfd_window_attn(q.cuda(), k.cuda(), v.cuda(), torch.tensor(pos, dtype=torch.int32,
+                              device="cuda"), kd, vd, 511)
+    torch.cuda.synchronize()
+    f = lambda t: t.float().numpy()
+    args = (np32(out), np32(kd), np32(vd), f(q), f(k), f(v), pos, f(kr), f(vr), 511)
+    check_window_attn(*args)
+    with pytest.raises(AssertionError):
+        check_window_attn(*args, rnd=trunc_bf16)

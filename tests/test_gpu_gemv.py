@@ -4,7 +4,8 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import (assert_bf16_close, assert_fp32_close, assert_sorted_keys, assert_topk_valid,
+from helpers import (assert_bf16_rounding, assert_fp32_close, assert_sorted_keys, assert_topk_valid,
+                     full_head_oracle, gemv_bf16_err,
                      need_gpu, np32, same_bits)
 from oracle import gemv as og
 from oracle.quant import quant_fp8_block32, quant_fp8_row
@@ -94,11 +95,10 @@ def test_output_modes(out_mode, wfmt):
     torch.cuda.synchronize()
     acc, S = oracle_acc_S(case, wfmt)
     if out_mode == tfd.OUT_BF16:
-        assert_bf16_close(np32(y), og.gemv(case["wo"], case["xo"], wfmt, case["so"], og.OUT_BF16))
+        assert_bf16_rounding(np32(y), acc, gemv_bf16_err(S), "out bf16")
     elif out_mode == tfd.OUT_ADD_BF16:
-        ref = og.gemv(case["wo"], case["xo"], wfmt, case["so"], og.OUT_ADD_BF16,
-                      res=res.float().numpy())
-        assert_bf16_close(np32(y), ref)
+        ex = res.float().numpy().astype(np.float64) + acc
+        assert_bf16_rounding(np32(y), ex, gemv_bf16_err(S, ex), "out added to bf16")
     else:
         assert y is None
     assert_topk_valid(np32(tv), ti.cpu().numpy(), acc, S, 1, what="top-1")
@@ -378,29 +378,11 @@ def test_add_bf16_in_place_on_a_strided_output():
     before = big.clone()
     tfd.tfd_head_gemv(case["w"], tfd.W_FP8_ROW, case["scales"], case["x"], tfd.OUT_ADD_BF16, y=y)
     torch.cuda.synchronize()
-    ref = og.gemv(case["wo"], case["xo"], og.W_FP8_ROW, case["so"], og.OUT_ADD_BF16,
-                  res=np32(before[:, 32:32 + n]))
-    assert_bf16_close(np32(y), ref)
+    acc, S = oracle_acc_S(case, tfd.W_FP8_ROW)
+    ex = np32(before[:, 32:32 + n]).astype(np.float64) + acc
+    assert_bf16_rounding(np32(y), ex, gemv_bf16_err(S, ex), "in place, strided")
     assert torch.equal(big[:, :32], before[:, :32]) and torch.equal(big[:, 32 + n:],
                                                                     before[:, 32 + n:])
-
-
-def full_head_oracle(w, x, wfmt=og.W_BF16, scales=None, chunk=16384):
-    """Oracle logits and S of the full head, computed a chunk of rows at a time."""
-    n = w.shape[0]
-    accs, Ss = [], []
-    for a in range(0, n, chunk):
-        b = min(n, a + chunk)
-        if wfmt == og.W_FP8_BLOCK32:
-            sc = scales[a // 32:b // 32]
-        elif wfmt == og.W_FP8_ROW:
-            sc = scales[a:b]
-        else:
-            sc = None
-        wc = w[a:b]
-        accs.append(og.gemv_acc(wc, x, wfmt, sc))
-        Ss.append(og.gemv_abs_scale(wc, x, wfmt, sc))
-    return np.concatenate(accs, axis=1), np.concatenate(Ss, axis=1)
 
 
 @pytest.fixture(scope="module")

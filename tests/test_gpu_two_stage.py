@@ -4,8 +4,9 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import assert_fp32_close, need_gpu, np32, same_bits
+from helpers import assert_fp32_close, assert_topk_valid, need_gpu, np32, same_bits
 from oracle import gemv as og
+from oracle.numerics import fl32
 from oracle.two_stage import rescore as oracle_rescore
 from oracle.topk import topk as oracle_topk
 from speculative_decoding_draft_row_gb300 import tfd
@@ -37,6 +38,14 @@ def check(a, b, w, x, cand_k):
     # candidates: bit-exact top-k of the GPU's z
     ov, oi = oracle_topk(np32(z), cand_k)
     assert np.array_equal(ci.cpu().numpy(), oi) and same_bits(np32(cv), ov)
+    # ... and a valid top-k of the oracle's own chain: z_o = A fl32(B x). The GPU's z differs
+    # from z_o by its own fp32 sums (1e-5 |A| |h|) and by A times the error of its h (1e-5 S_h
+    # each, plus the oracle's fl32 of h): S = |A| (1.01 |h_o| + S_h) bounds both
+    h_o = fl32(og.gemv_acc(bn, xn)).astype(np.float64)
+    z_o = og.gemv_acc(an, h_o)
+    S_z = np.abs(h_o) * 1.01 + og.gemv_abs_scale(bn, xn)
+    S_z = S_z @ np.abs(an.astype(np.float64)).T
+    assert_topk_valid(np32(cv), ci.cpu().numpy(), z_o, S_z, cand_k, what="candidates vs oracle z")
     # rescore of the GPU's candidates
     cand = ci.cpu().numpy()
     oe, _, _ = oracle_rescore(wn, xn, cand)

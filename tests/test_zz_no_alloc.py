@@ -1,6 +1,6 @@
-"""tfd_head_gemv_noalloc: the head GEMV for callers that cannot allocate device memory (graph
-capture regions, allocator-free serving loops, plugins without an allocator), running on the
-library's fixed scratch array. Checked through the C ABI against tfd_head_gemv with a caller
+"""tfd_head_gemv_noalloc: the head GEMV for callers that cannot allocate device memory (serving
+loops that keep cudaMalloc, which can block or synchronise the device, off the hot path; plugins
+whose host framework owns all device memory), running on the library's fixed scratch array. Checked through the C ABI against tfd_head_gemv with a caller
 workspace, on two calls in a row (the second must not see the first's leftovers). This file is
 collected last, and it also passes when run alone in a fresh process."""
 import numpy as np

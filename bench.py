@@ -777,6 +777,70 @@ def run_case(args):
           flush=True)
 
 
+def run_trace(args):
+    """Phase stamps of the head GEMV kernel from a build with -DTFD_TRACE=1 (built on first use
+    into _build/trace): per block the entry, the staged activations, the end of each group and
+    the end of the groups, summarised over the blocks of one call (ns). Reproduces the per-phase
+    figures quoted in the profiles."""
+    if os.environ.get("TFD_TRACE_CHILD") != "1":
+        from speculative_decoding_draft_row_gb300 import build
+        lib = build.build_library(extra_flags=["-DTFD_TRACE=1"],
+                                  build_dir=os.path.join(build.BUILD_DIR, "trace"))
+        env = dict(os.environ, TFD_LIBRARY=lib, TFD_TRACE_CHILD="1")
+        sys.exit(subprocess.run([sys.executable, os.path.abspath(__file__), *sys.argv[1:]],
+                                env=env, cwd=ROOT).returncode)
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    from speculative_decoding_draft_row_gb300 import tfd
+    from synth import inputs
+
+    torch.cuda.set_device(0)
+    fmt, rows, topk = args.trace.split(":")
+    rows, topk = int(rows), int(topk)
+    mode = {"bf16": tfd.W_BF16, "row": tfd.W_FP8_ROW, "block32": tfd.W_FP8_BLOCK32,
+            "block32il": tfd.W_FP8_BLOCK32_IL}[fmt]
+    w, _ = inputs.head(tie_frac=0.01)
+    wd = w.cuda()
+    del w
+    if mode == tfd.W_BF16:
+        codes, scales = wd, None
+    else:
+        codes, scales = tfd.tfd_quant_fp8(wd, mode)
+        del wd
+    x = inputs.rows(32)[:rows].cuda()
+    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(rows, VOCAB, max(topk, 1)))
+    buf = torch.zeros((1024, 64), dtype=torch.int64, device="cuda")
+    lib = tfd.library()
+    lib.tfd_trace_set.argtypes = [ctypes.c_void_p]
+    f = lambda: tfd.tfd_head_gemv(codes, mode, scales, x, tfd.OUT_NONE, topk=topk, ws=ws)
+    for _ in range(args.warmup):
+        f()
+    torch.cuda.synchronize()
+    lib.tfd_trace_set(buf.data_ptr())
+    f()
+    torch.cuda.synchronize()
+    lib.tfd_trace_set(None)
+    t = buf.cpu().numpy()
+    used = t[:, 0] > 0
+    t = t[used]
+    t0 = t[:, 0].min()
+    med = lambda v: float(statistics.median(v.tolist())) if len(v) else None
+    groups = [(t[b, 2:59][t[b, 2:59] > 0] - t[b, 1]) for b in range(len(t))]
+    per_group = [float((g[-1] - 0) / len(g)) for g in groups if len(g)]
+    out = {"case": f"{fmt} rows {rows} topk {topk}", "blocks": int(used.sum()),
+           "entry_skew_ns": float(t[:, 0].max() - t0),
+           "staging_ns_median": med(t[:, 1] - t[:, 0]), "staging_ns_max": float((t[:, 1] - t[:, 0]).max()),
+           "first_group_ns_median": med(t[:, 2] - t[:, 1]),
+           "group_ns_median": med(np.array(per_group)),
+           "groups_per_block": [int(min(len(g) for g in groups)), int(max(len(g) for g in groups))],
+           "groups_done_ns_min": float(t[:, 61].min() - t0), "groups_done_ns_max": float(t[:, 61].max() - t0),
+           "join_done_ns": float(t[:, 63].max() - t0) if (t[:, 63] > 0).any() else None}
+    print(json.dumps(out), flush=True)
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -826,13 +890,18 @@ def main():
                                        "rows17", "rows24", "rows32"],
                     default=None,
                     help="profiling case: one row of the path alone")
+    ap.add_argument("--trace", default=None, metavar="FMT:ROWS:TOPK",
+                    help="phase stamps of one head GEMV call from a -DTFD_TRACE=1 build, e.g. "
+                         "row:16:64 (FMT bf16, row, block32 or block32il)")
     ap.add_argument("--no-extras", action="store_true",
                     help="time the headline calls only (no e2e, FP8 or CPU baseline): a small "
                          "case for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.trace:
+        run_trace(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.fp8:
         run_fp8_case(args)

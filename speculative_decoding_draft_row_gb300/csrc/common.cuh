@@ -97,6 +97,29 @@ __device__ __forceinline__ uint2 ldg_stream8(const void* p, uint64_t pol) {
   return v;
 }
 
+// ---- phase timestamps (TFD_TRACE builds only) -----------------------------------------------------
+// A build with -DTFD_TRACE=1 records the global nanosecond timer at fixed points of a kernel, one
+// row of kTraceSlots stamps per block, into a caller-given device buffer (tfd_trace_set); the
+// default build compiles none of it.
+#ifndef TFD_TRACE
+#define TFD_TRACE 0
+#endif
+constexpr int kTraceSlots = 64;
+#if TFD_TRACE
+__device__ __forceinline__ void trace_stamp(uint64_t* buf, int slot) {
+  if (buf != nullptr && threadIdx.x == 0 && slot < kTraceSlots) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    buf[(int64_t)blockIdx.x * kTraceSlots + slot] = t;
+  }
+}
+#define TFD_STAMP(buf, slot) trace_stamp((buf), (slot))
+#else
+#define TFD_STAMP(buf, slot) \
+  do {                       \
+  } while (0)
+#endif
+
 // ---- warp reductions ----------------------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -139,9 +162,12 @@ namespace tfd_internal {
 // Top-k over fp32 logits by a threshold filter, one thread-block cluster per row (topk.cu). The
 // workspace is tfd_topk_workspace() bytes. pre_max, when not null, already holds the value key of
 // the maximum of every 16-logit sub-group of each row, [rows][ceil(n / 16)], so the logits are
-// read only where a sub-group can reach the threshold.
+// read only where a sub-group can reach the threshold. part_max, when not null, holds the value
+// key of the largest logit of each of `parts` contiguous parts of each row, [parts][rows]; with
+// k <= parts the threshold is then the k-th largest of those (one block per row).
 tfd_status topk_launch(const float* logits, int rows, int64_t n, int64_t ld, int k,
                        const int32_t* id_map, float* vals, int32_t* ids, int64_t ld_out,
-                       const uint32_t* pre_max, void* ws, size_t ws_bytes, cudaStream_t stream);
+                       const uint32_t* pre_max, const uint32_t* part_max, int parts, void* ws,
+                       size_t ws_bytes, cudaStream_t stream);
 size_t topk_workspace(int rows, int64_t n, int k);
 }  // namespace tfd_internal

@@ -11,9 +11,17 @@ TFD_GEMV_EXTERN(TFD_W_FP8_ROW)
 TFD_GEMV_EXTERN(TFD_W_FP8_BLOCK32)
 TFD_GEMV_EXTERN(TFD_W_FP8_BLOCK32_IL)
 
+// Groups taken from a queue in the workspace when there is one (1), or a static split (0).
+#ifndef TFD_GEMV_QUEUE
+#define TFD_GEMV_QUEUE 1
+#endif
+
 namespace {
 
 using namespace tfd_gemv;
+
+// The phase-stamp buffer of TFD_TRACE builds (set by tfd_trace_set; always null otherwise).
+uint64_t* g_trace = nullptr;
 
 // Whether a call's activation tile fits shared memory (with k split over a cluster if needed).
 bool gemv_fits(int wfmt, int xfmt, int rows, int64_t k) {
@@ -40,18 +48,20 @@ struct GemvWs {
   float2* part_ms;
   float* logits;
   uint32_t* submax;
+  uint32_t* part_max;
   void* topk_ws;
   size_t topk_bytes;
 };
 
 // Workspace: [counter | part keys for top-1 | fp32 logits for top-k > 1 | sub-group maxima for
-// top-k > 1 | top-k workspace].
+// top-k > 1 | part maxima for top-k > 1 | top-k workspace].
 size_t gemv_ws_layout(int rows, int64_t n, int topk, bool logits_in_y, char* base, GemvWs* out) {
   size_t off = 256;
   // top-1: per part a key and an online-softmax pair per row
   size_t keys = topk == 1 ? tfd_host::round_up((size_t)kMaxParts * rows * 8, 256) * 2 : 0;
   size_t lg = (topk > 1 && !logits_in_y) ? tfd_host::round_up((size_t)rows * n * 4, 256) : 0;
   size_t sub = topk > 1 ? tfd_host::round_up((size_t)rows * ((n + 15) / 16) * 4, 256) : 0;
+  size_t pm = topk > 1 ? tfd_host::round_up((size_t)kMaxParts * rows * 4, 256) : 0;
   size_t tk = topk > 1 ? tfd_internal::topk_workspace(rows, n, topk) : 0;
   if (out) {
     out->counter = reinterpret_cast<uint32_t*>(base);
@@ -59,11 +69,12 @@ size_t gemv_ws_layout(int rows, int64_t n, int topk, bool logits_in_y, char* bas
     out->part_ms = keys ? reinterpret_cast<float2*>(base + off + keys / 2) : nullptr;
     out->logits = lg ? reinterpret_cast<float*>(base + off + keys) : nullptr;
     out->submax = sub ? reinterpret_cast<uint32_t*>(base + off + keys + lg) : nullptr;
-    out->topk_ws = tk ? base + off + keys + lg + sub : nullptr;
+    out->part_max = pm ? reinterpret_cast<uint32_t*>(base + off + keys + lg + sub) : nullptr;
+    out->topk_ws = tk ? base + off + keys + lg + sub + pm : nullptr;
     out->topk_bytes = tk;
   }
   if (topk == 0) return 0;
-  return off + keys + lg + sub + tk;
+  return off + keys + lg + sub + pm + tk;
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -142,11 +153,21 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   a.logits = nullptr;
   a.ld_logits = 0;
   a.submax = nullptr;
+  a.part_max = nullptr;
   if (topk > 1) {
     a.logits = logits_in_y ? reinterpret_cast<float*>(y) : wl.logits;
     a.ld_logits = logits_in_y ? ldy : n;
     a.submax = wl.submax;
+    a.part_max = wl.part_max;
   }
+  int parts_used = 0;
+  a.parts_used = &parts_used;
+  a.trace = g_trace;
+  // groups taken from a queue in the workspace (bit-identical results; not with the confidence,
+  // whose merge order would then follow the blocks' shares)
+  a.queue = (TFD_GEMV_QUEUE && wl.counter != nullptr && need > 0 && top1_conf == nullptr)
+                ? wl.counter + 1
+                : nullptr;
   a.part_keys = wl.part_keys;
   a.counter = wl.counter;
   a.top_vals = top_vals;
@@ -164,5 +185,12 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   else st = gemv_launch_x<TFD_W_BF16>(a, xfmt, parts, s);
   if (st != TFD_OK || topk <= 1) return st;
   return tfd_internal::topk_launch(a.logits, rows, n, a.ld_logits, topk, id_map, top_vals, top_ids,
-                                   ldt, wl.submax, wl.topk_ws, wl.topk_bytes, s);
+                                   ldt, wl.submax, wl.part_max, parts_used, wl.topk_ws,
+                                   wl.topk_bytes, s);
 }
+
+#if TFD_TRACE
+// TFD_TRACE builds only (not part of the public header): the device buffer, [blocks][64] uint64,
+// that the head GEMV kernel writes its phase stamps into; NULL stops the recording.
+extern "C" void tfd_trace_set(void* dev_buf) { g_trace = reinterpret_cast<uint64_t*>(dev_buf); }
+#endif

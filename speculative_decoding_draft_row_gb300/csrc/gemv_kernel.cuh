@@ -68,6 +68,18 @@ constexpr int kPrefetchParts = 8;
 #ifndef TFD_GEMV_DEPTH_AQ_NT2
 #define TFD_GEMV_DEPTH_AQ_NT2 4
 #endif
+// Fast path for 4096-wide weights (the pages' hidden size) with 4 k-slices and no cluster split:
+// each k-slice's steps fully unrolled, every weight and activation address a base plus an
+// immediate, the ring's refills following statically into the next group, and no per-step range
+// checks (a block takes it when all of its groups lie inside the matrix).
+#ifndef TFD_GEMV_FAST
+#define TFD_GEMV_FAST 1
+#endif
+// 4096-wide activations staged with constant geometry by their own instantiation (1), or by the
+// general staging loop (0).
+#ifndef TFD_GEMV_STAGE4K
+#define TFD_GEMV_STAGE4K 1
+#endif
 // CUDA-core form of the bf16 x bf16 step (off by default): the same operands, multiplied with
 // fp32 FMAs instead of tensor-core MMAs. It exists to measure whether the tensor cores pay at this
 // row count; the library is built with it only for that measurement.
@@ -134,6 +146,7 @@ struct GemvArgs {
   float* logits;  // fp32 logits destination for topk > 1 (may equal y), else null
   int64_t ld_logits;
   uint32_t* submax;  // topk > 1: [rows][ceil(n / 16)] value key of each 16-row sub-group's max
+  uint32_t* part_max;  // topk > 1: [parts][rows] value key of each part's largest output
   uint64_t* part_keys;  // [parts][rows]
   uint32_t* counter;
   float* top_vals;
@@ -145,6 +158,9 @@ struct GemvArgs {
   int64_t ngroups;
   int ssl;  // steps per k slice
   int csplit;  // blocks of a cluster splitting k (1: no cluster); parts counts clusters
+  int* parts_used;  // host only (never read by the kernel): the launcher stores the part count
+  uint64_t* trace;  // TFD_TRACE builds: [blocks][kTraceSlots] phase stamps, or null
+  uint32_t* queue;  // group queue counter (zero between calls), or null for a static split
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -265,9 +281,10 @@ struct Layout {
     return KSL == 1 ? 0 : (size_t)2 * kWarps * NT * 32 * 16;
   }
   __host__ __device__ static size_t best_bytes() {
-    // block best keys, join keys, per-row x max and x scale, block (max, sum) pairs, join pairs
+    // block best keys, join keys, per-row x max and x scale, block (max, sum) pairs, join pairs,
+    // per-row part maxima
     return (size_t)MT * kMaxRowsPad * 8 + kMaxRowsPad * kWarps * 8 + 2 * kMaxRowsPad * 4 +
-           MT * kMaxRowsPad * 8 + kMaxRowsPad * kWarps * 8;
+           MT * kMaxRowsPad * 8 + kMaxRowsPad * kWarps * 8 + kMaxRowsPad * 4;
   }
   // group partials of a block for its cluster leader, double-buffered (4 k-slices only)
   __host__ __device__ static size_t cpart_bytes() {
@@ -278,9 +295,13 @@ struct Layout {
   }
 };
 
-template <int WF, int XF, int NT, int D, int KSL>
+// VAR: 0 the general form; 1 a 4096-wide matrix staged by one block (no cluster split) with bf16
+// activations: constant staging geometry; 2 that, plus the unrolled check-free weight loop (n a
+// multiple of the group rows). The host picks the instantiation.
+template <int WF, int XF, int NT, int D, int KSL, int VAR = 0>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? TFD_GEMV_MINB_NT1 : 1)
 gemv_kernel(const GemvArgs a) {
+  constexpr bool FASTP = VAR == 2;
   using L = Layout<WF, XF, NT, KSL>;
   constexpr int MT = L::MT;
   constexpr int GR = 16 * MT;  // rows per group
@@ -301,6 +322,7 @@ gemv_kernel(const GemvArgs a) {
   float* sxscale = reinterpret_cast<float*>(sxmax + kMaxRowsPad);
   float2* sms = reinterpret_cast<float2*>(sxscale + kMaxRowsPad);  // [MT][kMaxRowsPad]
   float2* sjms = sms + MT * kMaxRowsPad;                             // [kWarps][kMaxRowsPad]
+  uint32_t* spmax = reinterpret_cast<uint32_t*>(sjms + kWarps * kMaxRowsPad);  // [kMaxRowsPad]
   __shared__ int is_last;
   // FP8 weights run f16 MMAs: each activation row is scaled by a power of two 2^-e_r into f16 range
   // (max |x| in [2^14, 2^15)), which keeps every bf16 activation exact down to 2^-32 of the row's
@@ -313,6 +335,16 @@ gemv_kernel(const GemvArgs a) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int mt = warp % MT, ks = warp / MT;
+  // trace slots: 0 entry, 1 activations staged, 2 + j end of the block's group j (up to 57),
+  // 60 the SM, 61 groups done, 62 part keys written, 63 the join done (last block)
+  TFD_STAMP(a.trace, 0);
+#if TFD_TRACE
+  if (a.trace != nullptr && tid == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    a.trace[(int64_t)blockIdx.x * kTraceSlots + 60] = smid;
+  }
+#endif
   // Split k over a cluster (small vocabularies): block crank of cluster cid takes k-slices
   // 4 crank .. 4 crank + 3 of every group of the cluster; the leader (crank 0) sums the blocks'
   // partials in rank order and runs the epilogue.
@@ -333,11 +365,34 @@ gemv_kernel(const GemvArgs a) {
   const int64_t t_begin = KSL == 1 ? (int64_t)cid * ntiles / a.parts : 0;
   const int64_t t_end = KSL == 1 ? (int64_t)(cid + 1) * ntiles / a.parts : 0;
   const int64_t row_off = t_begin * 16;
-  const int64_t g_begin = KSL == 1 ? 0 : (int64_t)cid * a.ngroups / a.parts;
+  // The block's groups: with one k-slice, 0 .. g_end - 1 of its tile range; with 4 k-slices either
+  // the static range g_begin .. g_end - 1, or (a queue in the workspace, no cluster split, more
+  // than a ring's depth of steps per k-slice) group cid first and then the next unclaimed group
+  // of a queue shared by all blocks (parts + the counter's old value), so faster blocks take more
+  // groups and the blocks finish together. Group j of the sequence is published in s_q[j & 3]:
+  // the claiming thread (lane 0 of the last warp, never a reducer of the group epilogue when a
+  // queue is used, so the atomic's latency is off the critical path) claims groups 1 and 2
+  // before the first barrier and group j + 3 just after the barrier that ends group j, which is
+  // after every warp has read group j - 1's slot and before any needs group j + 3 (the ring
+  // enters group j + 1 during group j).
+  constexpr int64_t kNoGroup = (int64_t)1 << 40;
+  const bool dyn = KSL == 4 && NT <= 2 && csplit == 1 && a.queue != nullptr &&
+                   (ssl + D - 1) / D * D > D;
+  const bool claimer = warp == kWarps - 1 && lane == 0;
+  const int64_t g_begin = KSL == 1 ? 0 : dyn ? (int64_t)cid : (int64_t)cid * a.ngroups / a.parts;
   const int64_t g_end = KSL == 1 ? (t_end - t_begin + 15) / 16
-                                 : (int64_t)(cid + 1) * a.ngroups / a.parts;
-  auto tile_in = [&](int64_t gi, int tile) {  // the tile is in this block's range
-    return KSL == 1 ? t_begin + 16 * gi + tile < t_end : gi < g_end;
+                      : dyn ? a.ngroups : (int64_t)(cid + 1) * a.ngroups / a.parts;
+  __shared__ int64_t s_q[4];
+  auto claim = [&]() -> int64_t {
+    const int64_t v = (int64_t)a.parts + (int64_t)atomicAdd(a.queue, 1u);
+    return v < a.ngroups ? v : kNoGroup;
+  };
+  auto seq_group = [&](int j) -> int64_t {  // group j of this block's sequence, or kNoGroup
+    if (KSL == 4 && dyn) return j == 0 ? ((int64_t)cid < a.ngroups ? (int64_t)cid : kNoGroup) : s_q[j & 3];
+    return g_begin + j < g_end ? g_begin + j : kNoGroup;
+  };
+  auto tile_in = [&](int64_t gi, int tile) {  // the tile exists and is this block's
+    return KSL == 1 ? gi < kNoGroup && t_begin + 16 * gi + tile < t_end : gi < a.ngroups;
   };
   const int s_loc = ks * ssl;              // the k-slice's first step in shared memory
   const int s_begin = kstep0 + s_loc;      // ... and in the row
@@ -361,7 +416,9 @@ gemv_kernel(const GemvArgs a) {
   const int nvalid = steps_below(K - toff);
   const int nvalid_b = WF == TFD_W_FP8_BLOCK32 ? steps_below(K - 32 - toff) : nvalid;
 
-  // Load state: group, step, row pointer and row validity; addresses advance by a constant.
+  // Load state: group (and its place in the sequence), step, row pointer and row validity;
+  // addresses advance by a constant.
+  int ld_j = 0;
   int64_t ld_g = g_begin;
   int ld_s = 0;
   const unsigned char* lp = nullptr;
@@ -405,7 +462,7 @@ gemv_kernel(const GemvArgs a) {
       }
       lp += STEPK * EB;
       sp += 2;
-      if (++ld_s == ssl_loop) { ld_s = 0; ++ld_g; set_group(); }
+      if (++ld_s == ssl_loop) { ld_s = 0; ld_g = seq_group(++ld_j); set_group(); }
       return;
     }
 #pragma unroll
@@ -444,16 +501,68 @@ gemv_kernel(const GemvArgs a) {
     }
     lp += STEPK * EB;
     sp += 2;
-    if (++ld_s == ssl_loop) { ld_s = 0; ++ld_g; set_group(); }
+    if (++ld_s == ssl_loop) { ld_s = 0; ld_g = seq_group(++ld_j); set_group(); }
+  };
+
+  // Fast path (the FASTP instantiation, chosen on the host): k == 4096, 4 k-slices, no cluster
+  // split, n a multiple of the group rows.
+  constexpr int FK = 4096;
+  constexpr int SSLC = FK / (KSL * STEPK);  // steps per k-slice at k == FK
+  constexpr bool FASTK = FASTP && KSL == 4 && SSLC >= D;
+  constexpr int64_t FROWB = (int64_t)FK * EB;
+  const bool fast = FASTK && g_begin < g_end;
+  // this warp's first byte of group gi in the fast path, and its scale bytes (block-32 forms)
+  auto fast_ptr = [&](int64_t gi) {
+    return wbase + (gi * GR + mt * 16 + g) * FROWB + ((int64_t)s_begin * STEPK + toff) * EB;
+  };
+  auto fast_sp = [&](int64_t gi) {
+    return blk_scales + ((gi * GR + mt * 16) >> 5) * (FK / 32) + 2 * (int64_t)s_begin;
+  };
+  auto fload = [&](WLoad<WF>& b, const unsigned char* q, const uint8_t* sq) {
+    constexpr int64_t R8 = 8 * FROWB;  // row g + 8
+    if (WF == TFD_W_FP8_BLOCK32) {
+      uint2 v = ldg_stream8(q, wpol);
+      b.r[0][0] = v.x; b.r[0][1] = v.y;
+      v = ldg_stream8(q + 32, wpol);
+      b.r[0][2] = v.x; b.r[0][3] = v.y;
+      v = ldg_stream8(q + R8, wpol);
+      b.r[1][0] = v.x; b.r[1][1] = v.y;
+      v = ldg_stream8(q + R8 + 32, wpol);
+      b.r[1][2] = v.x; b.r[1][3] = v.y;
+    } else {
+      uint4 v = ldg_stream16(q, wpol);
+      b.r[0][0] = v.x; b.r[0][1] = v.y; b.r[0][2] = v.z; b.r[0][3] = v.w;
+      v = ldg_stream16(q + R8, wpol);
+      b.r[1][0] = v.x; b.r[1][1] = v.y; b.r[1][2] = v.z; b.r[1][3] = v.w;
+    }
+    if (BLK) b.scb = __ldg(reinterpret_cast<const uint16_t*>(sq));
+    else b.scb = 0u;
   };
 
   // The first D steps of weights are in flight while the activations are staged.
   WLoad<WF> buf[D];
+  auto prime = [&]() {
+    if constexpr (FASTK) {
+      if (fast) {
+        const unsigned char* q = fast_ptr(g_begin);
+        const uint8_t* sq = BLK ? fast_sp(g_begin) : nullptr;
 #pragma unroll
-  for (int i = 0; i < D; ++i) issue(buf[i]);
+        for (int i = 0; i < D; ++i) fload(buf[i], q + (int64_t)i * STEPK * EB, sq + 2 * i);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < D; ++i) issue(buf[i]);
+    }
+  };
+  // The ring's first steps are issued before the activations are staged, except where the staging
+  // keeps every row's chunk in registers (the 4096-wide form): there the L2 prefetch below covers
+  // the staging, and the ring follows it.
+  constexpr bool PRIME_LATE = VAR >= 1 && XF == TFD_X_BF16 && !AQ && NT <= 2;
+  if constexpr (!PRIME_LATE) prime();
   // Staging the activations takes longer than the ring's loads (every block reads all rows, which
   // all blocks want at once); meanwhile the first TFD_GEMV_PREFETCH bytes of the block's first
   // group are fetched into L2, so the weight stream does not pause.
+  auto l2_prefetch = [&]() {
   if (csplit == 1 && g_begin < g_end && tid < kPrefetchParts) {
     const int64_t row0 = row_off + g_begin * GR;
     const int64_t gbytes = (N - row0 < GR ? N - row0 : GR) * row_bytes;
@@ -466,171 +575,303 @@ gemv_kernel(const GemvArgs a) {
                    "r"((uint32_t)len)
                    : "memory");
   }
+  };
+  // (the 4096-wide staging issues its activation loads first, so they are not queued behind this)
+  if constexpr (VAR == 0 || !(XF == TFD_X_BF16 && !AQ && NT <= 2)) l2_prefetch();
 
   for (int i = tid; i < MT * kMaxRowsPad; i += kThreads) sbest[i] = 0ull;
-  if (tid < kMaxRowsPad) sxmax[tid] = 0u;
+  if (tid < kMaxRowsPad) { sxmax[tid] = 0u; spmax[tid] = 0u; }
+  if (dyn && claimer) {
+    s_q[1] = claim();
+    s_q[2] = claim();
+  }
   __syncthreads();
-  if (F16) {
-    // per-row max |x| over the whole row (non-negative floats order like their bit patterns): the
-    // chunks of all rows taken together, U loads in flight per thread; a warp whose lanes share a
-    // row takes its maximum and makes one shared atomic, otherwise each lane makes its own
-    constexpr int U = XF == TFD_X_F32 ? 4 : 8;
-    const int chunks = (int)(K / 8);
-    const int total = rows * chunks;
-    for (int base = 0; base < total; base += U * kThreads) {  // the same trip count in every lane
-      float m[U];
-      int rr[U];
-      if (XF != TFD_X_F32) {
-        uint4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int idx = base + u * kThreads + tid;
-          const bool ok = idx < total;
-          rr[u] = ok ? idx / chunks : 0;
-          v[u] = ok ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
-                                                     (int64_t)rr[u] * a.ldx + 8 * (idx - rr[u] * chunks))
-                    : make_uint4(0u, 0u, 0u, 0u);
+  // bf16 activations for FP8 weights: the raw rows are staged in one pass that also takes each
+  // row's max |x|; the power-of-two scaling into f16 is applied afterwards in shared memory. A
+  // block that stages only part of k (cluster split) takes the max over the whole row first.
+  constexpr bool ONEPASS_C = F16 && XF == TFD_X_BF16 && !AQ;
+  // 4096-wide bf16 activations staged whole by one block: 512 chunks of 8 a row, one per thread,
+  // so thread tid owns k = 8 tid .. 8 tid + 7 of every row (constant geometry, every row's load in
+  // flight at once, conversions in registers)
+  constexpr bool STAGE4K_C = VAR >= 1 && XF == TFD_X_BF16 && !AQ && NT <= 2 && kThreads * 8 == 4096;
+  constexpr bool stage4k = STAGE4K_C;
+  const bool onepass = ONEPASS_C && csplit == 1 && !stage4k;
+  if (F16 && !onepass && !stage4k) {
+    if (F16) {
+      // per-row max |x| over the whole row (non-negative floats order like their bit patterns): the
+      // chunks of all rows taken together, U loads in flight per thread; a warp whose lanes share a
+      // row takes its maximum and makes one shared atomic, otherwise each lane makes its own
+      constexpr int U = XF == TFD_X_F32 ? 4 : 8;
+      const int chunks = (int)(K / 8);
+      const int total = rows * chunks;
+      for (int base = 0; base < total; base += U * kThreads) {  // the same trip count in every lane
+        float m[U];
+        int rr[U];
+        if (XF != TFD_X_F32) {
+          uint4 v[U];
+  #pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int idx = base + u * kThreads + tid;
+            const bool ok = idx < total;
+            rr[u] = ok ? idx / chunks : 0;
+            v[u] = ok ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                                       (int64_t)rr[u] * a.ldx + 8 * (idx - rr[u] * chunks))
+                      : make_uint4(0u, 0u, 0u, 0u);
+          }
+  #pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            m[u] = 0.0f;
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) m[u] = fmaxf(m[u], fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+          }
+        } else {
+          float4 v[U][2];
+  #pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int idx = base + u * kThreads + tid;
+            const bool ok = idx < total;
+            rr[u] = ok ? idx / chunks : 0;
+            const float4* p = reinterpret_cast<const float4*>(
+                reinterpret_cast<const float*>(a.x) + (int64_t)rr[u] * a.ldx + 8 * (idx - rr[u] * chunks));
+            v[u][0] = ok ? p[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u][1] = ok ? p[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+  #pragma unroll
+          for (int u = 0; u < U; ++u) {
+            m[u] = 0.0f;
+  #pragma unroll
+            for (int h = 0; h < 2; ++h)
+              m[u] = fmaxf(m[u], fmaxf(fmaxf(fabsf(v[u][h].x), fabsf(v[u][h].y)),
+                                       fmaxf(fabsf(v[u][h].z), fabsf(v[u][h].w))));
+          }
         }
-#pragma unroll
+  #pragma unroll
         for (int u = 0; u < U; ++u) {
-          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-          m[u] = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) m[u] = fmaxf(m[u], fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-        }
-      } else {
-        float4 v[U][2];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int idx = base + u * kThreads + tid;
-          const bool ok = idx < total;
-          rr[u] = ok ? idx / chunks : 0;
-          const float4* p = reinterpret_cast<const float4*>(
-              reinterpret_cast<const float*>(a.x) + (int64_t)rr[u] * a.ldx + 8 * (idx - rr[u] * chunks));
-          v[u][0] = ok ? p[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[u][1] = ok ? p[1] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          m[u] = 0.0f;
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            m[u] = fmaxf(m[u], fmaxf(fmaxf(fabsf(v[u][h].x), fabsf(v[u][h].y)),
-                                     fmaxf(fabsf(v[u][h].z), fabsf(v[u][h].w))));
+          const int r0 = __shfl_sync(0xffffffffu, rr[u], 0);
+          if (__all_sync(0xffffffffu, rr[u] == r0)) {
+            const float mw = warp_max(m[u]);
+            if (lane == 0) atomicMax(&sxmax[r0], __float_as_uint(mw));
+          } else {
+            atomicMax(&sxmax[rr[u]], __float_as_uint(m[u]));
+          }
         }
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int r0 = __shfl_sync(0xffffffffu, rr[u], 0);
-        if (__all_sync(0xffffffffu, rr[u] == r0)) {
-          const float mw = warp_max(m[u]);
-          if (lane == 0) atomicMax(&sxmax[r0], __float_as_uint(mw));
-        } else {
-          atomicMax(&sxmax[rr[u]], __float_as_uint(m[u]));
+      __syncthreads();
+    }
+  }
+  auto row_scales_from_max = [&]() {
+    if (tid < kMaxRowsPad) {
+      if (AQ) {  // the row's E4M3 scale s = amax / 448 (IEEE division): epilogue factor and divisor
+        const float sx = __fdiv_rn(__uint_as_float(sxmax[tid]), 448.0f);
+        sxscale[tid] = sx;
+        sxmax[tid] = __float_as_uint(sx);
+      } else {
+        int e = 0;
+        const uint32_t ef = (sxmax[tid] >> 23) & 0xFFu;
+        if (F16 && sxmax[tid] != 0u && ef != 0xFFu) {
+          e = (int)ef - 127 - 14;
+          e = e < -110 ? -110 : (e > 110 ? 110 : e);
         }
+        sxscale[tid] = __uint_as_float((uint32_t)(e + 127) << 23);  // 2^e
+        sxmax[tid] = (uint32_t)(127 - e) << 23;                       // bits of 2^-e
       }
     }
     __syncthreads();
-  }
-  if (tid < kMaxRowsPad) {
-    if (AQ) {  // the row's E4M3 scale s = amax / 448 (IEEE division): epilogue factor and divisor
-      const float sx = __fdiv_rn(__uint_as_float(sxmax[tid]), 448.0f);
-      sxscale[tid] = sx;
-      sxmax[tid] = __float_as_uint(sx);
-    } else {
-      int e = 0;
-      const uint32_t ef = (sxmax[tid] >> 23) & 0xFFu;
-      if (F16 && sxmax[tid] != 0u && ef != 0xFFu) {
-        e = (int)ef - 127 - 14;
-        e = e < -110 ? -110 : (e > 110 ? 110 : e);
-      }
-      sxscale[tid] = __uint_as_float((uint32_t)(e + 127) << 23);  // 2^e
-      sxmax[tid] = (uint32_t)(127 - e) << 23;                       // bits of 2^-e
-    }
-  }
-  __syncthreads();
+  };
+  if (!onepass && !stage4k) row_scales_from_max();
   // ---- activations -> shared memory, in MMA B-fragment order ----
+  if constexpr (STAGE4K_C) {
+    const int k0 = 8 * tid;
+    const int s = k0 / STEPK;
+    const int rem = k0 - s * STEPK;
+    const int tt = BLK ? (rem & 31) >> 3 : rem / E;
+    const int hf = BLK ? rem >> 5 : (rem - tt * E) >> 3;
+    uint4 v[8 * NT];
+#pragma unroll
+    for (int r = 0; r < 8 * NT; ++r)
+      v[r] = r < rows ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                                        (int64_t)r * a.ldx + k0)
+                      : make_uint4(0u, 0u, 0u, 0u);
+    l2_prefetch();
+    if (F16) {
+      // each row's max |x| (non-negative floats order like their bit patterns): a warp maximum,
+      // one shared atomic per warp and row
+#pragma unroll
+      for (int r = 0; r < 8 * NT; ++r) {
+        if (r < rows) {  // block-uniform
+          const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+          uint32_t m = 0u;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            m = max(m, max((w[i] << 16) & 0x7FFFFFFFu, w[i] & 0x7FFF0000u));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == 0 && m != 0u) atomicMax(&sxmax[r], m);
+        }
+      }
+      __syncthreads();
+      row_scales_from_max();
+      // scaled by the row's 2^-e into f16 (exact for every bf16 down to 2^-32 of the row's max)
+#pragma unroll
+      for (int r = 0; r < 8 * NT; ++r) {
+        const float inv = __uint_as_float(sxmax[r]);
+        const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          asm("cvt.rn.f16x2.f32 %0, %1, %2;"
+              : "=r"(o[j])
+              : "f"(bf16_hi(w[j]) * inv), "f"(bf16_lo(w[j]) * inv));
+        }
+        v[r] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 8 * NT; ++r) xs[((s * NT + (r >> 3)) * H + hf) * 32 + (r & 7) * 4 + tt] = v[r];
+  } else
+  // Chunk idx (8 consecutive k of one activation row) goes to one 16-byte fragment slot; XU chunks a
+  // thread are loaded before any is stored, and each block starts at its own offset, so the blocks
+  // do not all ask for the same lines of the activations at once.
   {
     const int chunks_per_row = spad * STEPK / 8;
     const int total = 8 * NT * chunks_per_row;
-    for (int idx = tid; idx < total; idx += kThreads) {
-      const int r = idx / chunks_per_row;
-      const int c = idx - r * chunks_per_row;
-      const int k0 = c * 8;  // within the block's k range
-      const int s = k0 / STEPK;
-      const int rem = k0 - s * STEPK;
-      const int64_t kg = (int64_t)kstep0 * STEPK + k0;  // in the whole row
-      // A thread's 16-element chunk is contiguous, except in the block-32 form, where it is 8 elements
-      // of each 32-wide scale block of the step (so every MMA stays inside one block).
-      const int tt = BLK ? (rem & 31) >> 3 : rem / E;
-      const int hf = BLK ? rem >> 5 : (rem - tt * E) >> 3;
-      const int ln = (r & 7) * 4 + tt;
-      const int nt = r >> 3;
-      const bool ok = r < rows && kg < K;
-      const float inv = F16 ? __uint_as_float(sxmax[r]) : 1.0f;
-      if (AQ) {
-        // 8 codes: code = e4m3(fl32(x / s)), s = 0 for a zero row (its codes are zero)
-        uint32_t w0 = 0u, w1 = 0u;
-        if (ok) {
-          const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+    const int rot = (int)(((int64_t)blockIdx.x * 2053) % total);
+    constexpr int XU = XF == TFD_X_F32 ? 4 : 8;
+    for (int base = 0; base < total; base += XU * kThreads) {  // the same trip count in every lane
+      uint4 raw[XU][XF == TFD_X_F32 ? 2 : 1];
+      int cidx[XU];
+#pragma unroll
+      for (int u = 0; u < XU; ++u) {
+        int idx = base + u * kThreads + tid;
+        const bool in = idx < total;
+        idx += rot;
+        if (idx >= total) idx -= total;
+        cidx[u] = in ? idx : -1;
+        const int r = idx / chunks_per_row;
+        const int64_t kg = (int64_t)kstep0 * STEPK + (int64_t)(idx - r * chunks_per_row) * 8;
+        const bool ok = in && r < rows && kg < K;
+        if (XF == TFD_X_F32) {
+          const uint4* p = reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(a.x) +
                                                           (int64_t)r * a.ldx + kg);
-          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+          raw[u][0] = ok ? p[0] : make_uint4(0u, 0u, 0u, 0u);
+          raw[u][XF == TFD_X_F32 ? 1 : 0] = ok ? p[1] : make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          raw[u][0] = ok ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                                         (int64_t)r * a.ldx + kg)
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < XU; ++u) {
+        const int idx = cidx[u];
+        const int r = idx / chunks_per_row;
+        const int c = idx - r * chunks_per_row;
+        const int k0 = c * 8;  // within the block's k range
+        const int s = k0 / STEPK;
+        const int rem = k0 - s * STEPK;
+        // A thread's 16-element chunk is contiguous, except in the block-32 form, where it is 8
+        // elements of each 32-wide scale block of the step (so every MMA stays inside one block).
+        const int tt = BLK ? (rem & 31) >> 3 : rem / E;
+        const int hf = BLK ? rem >> 5 : (rem - tt * E) >> 3;
+        const int ln = (r & 7) * 4 + tt;
+        const int nt = r >> 3;
+        const uint4 v = raw[u][0];
+        if (ONEPASS_C && onepass) {  // block-uniform
+          // raw bf16 bits in the f16 slot; the row's max |x| (non-negative floats order like
+          // their bit patterns), one shared atomic per warp whose lanes share a row
+          uint32_t m = 0u;
+          const int rr = idx >= 0 ? r : -1;
+          if (idx >= 0) {
+            xs[((s * NT + nt) * H + hf) * 32 + ln] = v;
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              m = max(m, max((w[i] << 16) & 0x7FFFFFFFu, w[i] & 0x7FFF0000u));
+          }
+          const int r0 = __shfl_sync(0xffffffffu, rr, 0);
+          if (__all_sync(0xffffffffu, rr == r0)) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0 && r0 >= 0 && m != 0u) atomicMax(&sxmax[r0], m);
+          } else if (rr >= 0 && m != 0u) {
+            atomicMax(&sxmax[rr], m);
+          }
+          continue;
+        }
+        if (idx < 0) continue;
+        if (AQ) {
+          // 8 codes: code = e4m3(fl32(x / s)), s = 0 for a zero row (its codes are zero)
+          const float inv = __uint_as_float(sxmax[r]);
+          const uint32_t uw[4] = {v.x, v.y, v.z, v.w};
           uint32_t q[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            float lo = bf16_lo(u[i]), hi = bf16_hi(u[i]);
+            float lo = bf16_lo(uw[i]), hi = bf16_hi(uw[i]);
             if (inv > 0.0f) { lo = __fdiv_rn(lo, inv); hi = __fdiv_rn(hi, inv); }
             q[i] = f32x2_to_e4m3x2(lo, hi);
           }
-          w0 = q[0] | (q[1] << 16);
-          w1 = q[2] | (q[3] << 16);
-        }
-        reinterpret_cast<uint2*>(xs)[((s * NT + nt) * 32 + ln) * 2 + hf] = make_uint2(w0, w1);
-      } else if (XF == TFD_X_BF16 && !F16) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (ok)
-          v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
-                                              (int64_t)r * a.ldx + kg);
-        xs[((s * NT + nt) * H + hf) * 32 + ln] = v;
-      } else {
-        float f[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = 0.0f;
-        if (ok) {
+          reinterpret_cast<uint2*>(xs)[((s * NT + nt) * 32 + ln) * 2 + hf] =
+              make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+        } else if (XF == TFD_X_BF16 && !F16) {
+          xs[((s * NT + nt) * H + hf) * 32 + ln] = v;
+        } else {
+          const float inv = F16 ? __uint_as_float(sxmax[r]) : 1.0f;
+          float f[8];
           if (XF == TFD_X_BF16) {
-            uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
-                                                      (int64_t)r * a.ldx + kg);
-            uint32_t u[4] = {v.x, v.y, v.z, v.w};
+            const uint32_t uw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) { f[2 * i] = bf16_lo(u[i]); f[2 * i + 1] = bf16_hi(u[i]); }
+            for (int i = 0; i < 4; ++i) { f[2 * i] = bf16_lo(uw[i]); f[2 * i + 1] = bf16_hi(uw[i]); }
           } else {
-            const float4* p = reinterpret_cast<const float4*>(
-                reinterpret_cast<const float*>(a.x) + (int64_t)r * a.ldx + kg);
-            float4 u = p[0], w = p[1];
-            f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
-            f[4] = w.x; f[5] = w.y; f[6] = w.z; f[7] = w.w;
+            const uint4 v2 = raw[u][XF == TFD_X_F32 ? 1 : 0];
+            f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+            f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+            f[4] = __uint_as_float(v2.x); f[5] = __uint_as_float(v2.y);
+            f[6] = __uint_as_float(v2.z); f[7] = __uint_as_float(v2.w);
+          }
+          uint16_t h[3][8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (PL == 1) h[0][e] = f32_to_f16_bits(f[e] * inv);   // bf16 x, FP8 weights
+            else split3<F16>(f[e] * inv, h[0][e], h[1][e], h[2][e]);
+          }
+#pragma unroll
+          for (int pl = 0; pl < PL; ++pl) {
+            uint4 o;
+            o.x = h[pl][0] | ((uint32_t)h[pl][1] << 16);
+            o.y = h[pl][2] | ((uint32_t)h[pl][3] << 16);
+            o.z = h[pl][4] | ((uint32_t)h[pl][5] << 16);
+            o.w = h[pl][6] | ((uint32_t)h[pl][7] << 16);
+            xs[(((pl * spad + s) * NT + nt) * H + hf) * 32 + ln] = o;
           }
         }
-        uint16_t h[3][8];
+      }
+    }
+    if (ONEPASS_C && onepass) {
+      __syncthreads();  // every row's max |x| and every raw chunk is in shared memory
+      row_scales_from_max();
+      // each slot scaled by its row's 2^-e and rounded to f16 (exact for every bf16 down to
+      // 2^-32 of the row's max); a slot's row is (lane slot / 4) + 8 n-tile
+      const int slots = spad * NT * H * 32;
+      for (int i = tid; i < slots; i += kThreads) {
+        const int ln = i & 31;
+        const int nt = (i / (H * 32)) % NT;
+        const int r = nt * 8 + (ln >> 2);
+        const float inv = __uint_as_float(sxmax[r]);
+        const uint4 v = xs[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (PL == 1) h[0][e] = f32_to_f16_bits(f[e] * inv);   // bf16 x, FP8 weights
-          else split3<F16>(f[e] * inv, h[0][e], h[1][e], h[2][e]);
-        }
-#pragma unroll
-        for (int pl = 0; pl < PL; ++pl) {
-          uint4 v;
-          v.x = h[pl][0] | ((uint32_t)h[pl][1] << 16);
-          v.y = h[pl][2] | ((uint32_t)h[pl][3] << 16);
-          v.z = h[pl][4] | ((uint32_t)h[pl][5] << 16);
-          v.w = h[pl][6] | ((uint32_t)h[pl][7] << 16);
-          xs[(((pl * spad + s) * NT + nt) * H + hf) * 32 + ln] = v;
-        }
+        for (int j = 0; j < 4; ++j)
+          o[j] = (uint32_t)f32_to_f16_bits(bf16_lo(w[j]) * inv) |
+                 ((uint32_t)f32_to_f16_bits(bf16_hi(w[j]) * inv) << 16);
+        xs[i] = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
   }
   __syncthreads();
-
+  if constexpr (PRIME_LATE) prime();
+  TFD_STAMP(a.trace, 1);
 
   // One step: MMA j of the step takes elements [4j, 4j + 4) of each thread's chunk. All activation
   // fragments of the step are read first; each weight fragment is widened just before its MMAs.
@@ -778,10 +1019,10 @@ gemv_kernel(const GemvArgs a) {
   for (int i = 0; i < BS; ++i) ms[i] = make_float2(-INFINITY, 0.0f);
   const bool want_conf = a.topk == 1 && a.top1_conf != nullptr;
   // Returns the stored value (NaN outside the output).
-  auto epi = [&](int64_t row, int act, float v, int slot) -> float {
+  auto epi = [&](int64_t row, int act, float v, int slot, float rsc) -> float {
     if (row >= N || act >= rows) return __uint_as_float(0x7FC00000u);
     if (F16) v *= sxscale[act];
-    if (WF == TFD_W_FP8_ROW) v *= __ldg(row_scales + row);
+    if (WF == TFD_W_FP8_ROW) v *= rsc;
     const int64_t yi = (int64_t)act * a.ldy + row;
     if (a.out_mode == TFD_OUT_F32) {
       reinterpret_cast<float*>(a.y)[yi] = v;
@@ -810,13 +1051,25 @@ gemv_kernel(const GemvArgs a) {
 
   // Epilogue of one finished MMA tile (rows g, g + 8 of tile `tile` of group gi; activations act0,
   // act0 + 1), and the tile's sub-group maximum for a later top-k.
+  // row scales of the warp's own tile in the current group, loaded at the group's start (fast path)
+  float rs_pref[2] = {0.0f, 0.0f};
   auto finish_tile = [&](int64_t gi, int tile, int act0, float4 v, int slot0) {
     if (!tile_in(gi, tile)) return;  // warp-uniform: the tile belongs to the next block
     const int64_t row_lo = row_off + gi * GR + tile * 16 + g;
-    const float o0 = epi(row_lo, act0, v.x, slot0);
-    const float o1 = epi(row_lo, act0 + 1, v.y, slot0 + 1);
-    const float o2 = epi(row_lo + 8, act0, v.z, slot0);
-    const float o3 = epi(row_lo + 8, act0 + 1, v.w, slot0 + 1);
+    float rs0 = 1.0f, rs1 = 1.0f;
+    if (WF == TFD_W_FP8_ROW) {
+      if (FASTK && tile == mt) {
+        rs0 = rs_pref[0];
+        rs1 = rs_pref[1];
+      } else {
+        rs0 = row_lo < N ? __ldg(row_scales + row_lo) : 0.0f;
+        rs1 = row_lo + 8 < N ? __ldg(row_scales + row_lo + 8) : 0.0f;
+      }
+    }
+    const float o0 = epi(row_lo, act0, v.x, slot0, rs0);
+    const float o1 = epi(row_lo, act0 + 1, v.y, slot0 + 1, rs0);
+    const float o2 = epi(row_lo + 8, act0, v.z, slot0, rs1);
+    const float o3 = epi(row_lo + 8, act0 + 1, v.w, slot0 + 1, rs1);
     if (a.submax != nullptr) {
       // the 16 rows of this MMA tile are one sub-group: rows g and g + 8 of the eight lanes that
       // share t
@@ -832,6 +1085,10 @@ gemv_kernel(const GemvArgs a) {
       if (g == 0 && sg < S) {
         if (act0 < rows) a.submax[(int64_t)act0 * S + sg] = m0;
         if (act0 + 1 < rows) a.submax[(int64_t)(act0 + 1) * S + sg] = m1;
+        if (a.part_max != nullptr) {  // the part's maximum of each row
+          if (act0 < rows) atomicMax(&spmax[act0], m0);
+          if (act0 + 1 < rows) atomicMax(&spmax[act0 + 1], m1);
+        }
       }
     }
   };
@@ -843,15 +1100,8 @@ gemv_kernel(const GemvArgs a) {
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
   int rb = 0;
   const int mr = warp & 3, nr = warp >> 2;  // reducer role of warps < 4 * NT
-  for (int64_t gi = g_begin; gi < g_end; ++gi) {
-    for (int s0 = 0; s0 < ssl_loop; s0 += D) {
-#pragma unroll
-      for (int st = 0; st < D; ++st) {
-        // an empty step (past ssl) reads any valid activation slot: its weights are zero
-        compute(buf[st], s_loc + (s0 + st < ssl ? s0 + st : 0), acc);
-        issue(buf[st]);
-      }
-    }
+  // The end of group gi: k-slice partials summed, epilogue.
+  auto group_end = [&](int64_t gi, int j) {
     if constexpr (FFMA) {
       // sum over the four lanes of each weight row, then lane t keeps columns 2t, 2t + 1 of each
       // n-tile, as the MMA accumulator holds them
@@ -896,6 +1146,7 @@ gemv_kernel(const GemvArgs a) {
       for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
     }
     __syncthreads();
+    if (dyn && claimer) s_q[(j + 3) & 3] = claim();
     if (warp < 4 * NT) {
       // warp index = ks * 4 + mt, so the partials of row tile mr are warps mr, 4+mr, 8+mr, 12+mr.
       float4 v = red[((rb * kWarps + mr) * NT + nr) * 32 + lane];
@@ -921,12 +1172,66 @@ gemv_kernel(const GemvArgs a) {
     }
     }
     rb ^= 1;
+    TFD_STAMP(a.trace, 2 + (j < 57 ? j : 57));
+  };
+  if constexpr (FASTK) {
+    for (int j = 0;; ++j) {
+      const int64_t gi = seq_group(j);
+      if (gi >= kNoGroup) break;  // block-uniform
+      const int64_t gn = seq_group(j + 1);
+      const bool nxt = gn < kNoGroup;  // warp-uniform
+      const unsigned char* q = fast_ptr(gi);
+      const unsigned char* qn = fast_ptr(nxt ? gn : gi);
+      const uint8_t* sq = BLK ? fast_sp(gi) : nullptr;
+      const uint8_t* sqn = BLK ? fast_sp(nxt ? gn : gi) : nullptr;
+      if (WF == TFD_W_FP8_ROW) {
+        rs_pref[0] = __ldg(row_scales + gi * GR + mt * 16 + g);
+        rs_pref[1] = __ldg(row_scales + gi * GR + mt * 16 + g + 8);
+      }
+#pragma unroll
+      for (int st = 0; st < SSLC; ++st) {
+        compute(buf[st % D], s_loc + st, acc);
+        const int s2 = st + D;  // the step this ring slot takes next
+        if (s2 < SSLC)
+          fload(buf[st % D], q + (int64_t)s2 * STEPK * EB, sq + 2 * s2);
+        else if (nxt)
+          fload(buf[st % D], qn + (int64_t)(s2 - SSLC) * STEPK * EB, sqn + 2 * (s2 - SSLC));
+      }
+      group_end(gi, j);
+    }
+  } else {
+    for (int j = 0;; ++j) {
+      const int64_t gi = seq_group(j);
+      if (gi >= kNoGroup) break;  // block-uniform
+      for (int s0 = 0; s0 < ssl_loop; s0 += D) {
+#pragma unroll
+        for (int st = 0; st < D; ++st) {
+          // an empty step (past ssl) reads any valid activation slot: its weights are zero
+          compute(buf[st], s_loc + (s0 + st < ssl ? s0 + st : 0), acc);
+          issue(buf[st]);
+        }
+      }
+      group_end(gi, j);
+    }
   }
   if (csplit > 1) {
     cg::this_cluster().sync();  // the leader has read every block's last partial
     if (crank != 0) return;
   }
 
+  TFD_STAMP(a.trace, 61);
+  if (dyn && a.topk != 1) {
+    // the last block to finish (every claim of every block is done) zeroes the queue
+    __threadfence();
+    if (tid == 0 && atomicAdd(a.counter, 1u) == (uint32_t)(a.parts - 1)) {
+      *a.counter = 0u;
+      *a.queue = 0u;
+    }
+  }
+  if (a.part_max != nullptr) {
+    __syncthreads();  // every tile's maximum is in spmax
+    if (tid < rows) a.part_max[(int64_t)cid * rows + tid] = spmax[tid];
+  }
   if (a.topk != 1) return;
   // ---- top-1: block best per row, then the last block to finish joins the parts ----
   if (KSL == 1 || warp < 4 * NT) {
@@ -965,6 +1270,7 @@ gemv_kernel(const GemvArgs a) {
   if (tid < kMaxRowsPad) sjoin[tid] = 0ull;
   __threadfence();
   __syncthreads();
+  TFD_STAMP(a.trace, 62);
   if (tid == 0) is_last = (atomicAdd(a.counter, 1u) == (uint32_t)(a.parts - 1));
   __syncthreads();
   if (!is_last) return;
@@ -1013,7 +1319,11 @@ gemv_kernel(const GemvArgs a) {
       a.top1_conf[tid] = q.y > 0.0f ? 1.0f / q.y : __uint_as_float(0x7FC00000u);
     }
   }
-  if (tid == 0) *a.counter = 0u;  // leave the workspace zeroed
+  if (tid == 0) {  // leave the workspace zeroed
+    *a.counter = 0u;
+    if (dyn) *a.queue = 0u;
+  }
+  TFD_STAMP(a.trace, 63);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1089,8 +1399,32 @@ tfd_status gemv_launch_k(GemvArgs a, int parts_req, cudaStream_t stream) {
   }
   a.parts = parts;
   a.csplit = csplit;
+  if (a.parts_used != nullptr) *a.parts_used = parts;
   if (csplit == 1) {
     a.ssl = ssl;
+#if TFD_GEMV_STAGE4K
+    // (not the block-32 forms at two n-tiles: they spill in that instantiation)
+    if constexpr (XF == TFD_X_BF16 && KSL == 4 &&
+                  (NT == 1 || (NT == 2 && (WF == TFD_W_BF16 || WF == TFD_W_FP8_ROW)))) {
+      if (a.k == 4096) {  // staged by one block with constant geometry
+        auto k4 = gemv_kernel<WF, XF, NT, gemv_depth<WF, NT, XF>(), KSL, 1>;
+#if TFD_GEMV_FAST
+        // measured faster for one n-tile of bf16 and row-scaled FP8 weights only (the block-32
+        // forms spill when unrolled; two n-tiles gained nothing)
+        if constexpr (KSL == 4 && NT == 1 && (WF == TFD_W_BF16 || WF == TFD_W_FP8_ROW) &&
+                      4096 / (KSL * 4 * WTraits<WF>::E) >= gemv_depth<WF, NT, XF>()) {
+          // whole 64-row groups: the unrolled, check-free instantiation
+          if (a.n % (16 * (16 / KSL)) == 0) k4 = gemv_kernel<WF, XF, NT, gemv_depth<WF, NT, XF>(), KSL, 2>;
+        }
+#endif
+        if (cudaFuncSetAttribute(k4, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemLimit) != cudaSuccess)
+          return TFD_ERR_CUDA;
+        k4<<<parts, kThreads, smem, stream>>>(a);
+        return tfd_host::launch_status();
+      }
+    }
+#endif
     kern<<<parts, kThreads, smem, stream>>>(a);
     return tfd_host::launch_status();
   }

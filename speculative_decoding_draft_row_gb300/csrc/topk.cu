@@ -35,6 +35,11 @@ constexpr int kCandCap = 4096;             // keys of block 0's candidate list
 constexpr int kSubCap = 4096;              // sub-group maxima a block keeps in shared memory
 constexpr int kRankMax = 192;              // lists up to this length are ranked, else sorted
 constexpr int kRange = kBins / kCl;        // histogram bins each block sums: 512
+// Fused top-k after a GEMV that gives part maxima: threshold from them, one block per row (1), or
+// the cluster's histogram of sub-group maxima (0).
+#ifndef TFD_TOPK_PARTS
+#define TFD_TOPK_PARTS 1
+#endif
 
 struct ClusterSmem {
   uint64_t cand[kCandCap];     // block 0: the row's candidate keys
@@ -183,7 +188,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t n, int64_t ld, int
                     const int32_t* __restrict__ id_map, float* __restrict__ vals,
                     int32_t* __restrict__ ids, int64_t ld_out,
                     const uint32_t* __restrict__ pre_max, uint32_t* __restrict__ gmaxima,
-                    int64_t chunk) {
+                    int64_t chunk, const uint32_t* __restrict__ part_max, int parts) {
   extern __shared__ __align__(16) unsigned char tk_smem[];
   ClusterSmem& sm = *reinterpret_cast<ClusterSmem*>(tk_smem);
   cg::cluster_group cluster = cg::this_cluster();
@@ -231,14 +236,36 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t n, int64_t ld, int
       lmax = max(lmax, m);
     }
   }
-  const uint32_t bm = block_reduce_u32(lmax, true, sm);
-  if (tid == 0) sm.bmax = bm;
-  cluster.sync();  // maxima, block maxima and block 0's zeroed count are visible
+  uint32_t T;
+  if (part_max != nullptr) {
+    // ---- the threshold from the producer's part maxima, in every block: T = the k-th largest
+    // of them (k <= parts), the value v with (# > v) < k <= (# >= v) ----
+    uint32_t* pm = sm.hist;
+    for (int i = tid; i < parts; i += kThreads) pm[i] = __ldcg(part_max + (int64_t)i * gridDim.y + r);
+    if (tid == 0) sm.res_bin = 0;
+    __syncthreads();
+    for (int i = tid; i < parts; i += kThreads) {
+      const uint32_t v = pm[i];
+      int gt = 0, ge = 0;
+      for (int j = 0; j < parts; ++j) {
+        const uint32_t x = pm[j];
+        gt += x > v;
+        ge += x >= v;
+      }
+      if (gt < k && ge >= k) sm.res_bin = (int)v;  // every writer writes the same value
+    }
+    cluster.sync();  // maxima, the threshold and block 0's zeroed count are visible
+    T = (uint32_t)sm.res_bin;
+  } else {
+    const uint32_t bm = block_reduce_u32(lmax, true, sm);
+    if (tid == 0) sm.bmax = bm;
+    cluster.sync();  // maxima, block maxima and block 0's zeroed count are visible
 
-  // ---- the threshold T <= m_k ----
-  uint32_t K = 0u;
-  for (int q = 0; q < kCl; ++q) K = max(K, *cluster.map_shared_rank(&sm.bmax, q));
-  const uint32_t T = S >= k ? cluster_threshold(maxima, nsub, K, k, sm) : 0u;
+    // ---- the threshold T <= m_k ----
+    uint32_t K = 0u;
+    for (int q = 0; q < kCl; ++q) K = max(K, *cluster.map_shared_rank(&sm.bmax, q));
+    T = S >= k ? cluster_threshold(maxima, nsub, K, k, sm) : 0u;
+  }
 
   // ---- pass 2: the logits >= T of the sub-groups whose maximum reaches T ----
   uint64_t* cand0 = cluster.map_shared_rank(sm.cand, 0);
@@ -335,11 +362,15 @@ size_t topk_workspace(int rows, int64_t n, int k) {
 
 tfd_status topk_launch(const float* logits, int rows, int64_t n, int64_t ld, int k,
                        const int32_t* id_map, float* vals, int32_t* ids, int64_t ld_out,
-                       const uint32_t* pre_max, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                       const uint32_t* pre_max, const uint32_t* part_max, int parts, void* ws,
+                       size_t ws_bytes, cudaStream_t stream) {
   const size_t need = topk_workspace(rows, n, k);
   if (need == 0) return TFD_ERR_INVALID;
   if (ws == nullptr || ws_bytes < need) return TFD_ERR_WORKSPACE;
   const bool vec = tfd_host::aligned(logits, 16) && ld % 4 == 0;
+  // the producer's part maxima give the threshold when there are at least k parts
+  const bool use_parts = TFD_TOPK_PARTS && pre_max != nullptr && part_max != nullptr &&
+                         k <= parts && parts <= kBins;
   const size_t smem = sizeof(ClusterSmem);
   auto kern = vec ? topk_cluster_kernel<true> : topk_cluster_kernel<false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -347,7 +378,8 @@ tfd_status topk_launch(const float* logits, int rows, int64_t n, int64_t ld, int
     return TFD_ERR_CUDA;
   dim3 grid(kCl, (unsigned)rows);
   kern<<<grid, kThreads, smem, stream>>>(logits, n, ld, k, id_map, vals, ids, ld_out, pre_max,
-                                         reinterpret_cast<uint32_t*>(ws), part_len(n));
+                                         reinterpret_cast<uint32_t*>(ws), part_len(n),
+                                         use_parts ? part_max : nullptr, use_parts ? parts : 0);
   return tfd_host::launch_status();
 }
 
@@ -367,7 +399,6 @@ extern "C" tfd_status tfd_topk(const float* logits, int rows, int64_t n, int64_t
   if (!aligned(logits, 4) || !aligned(vals, 4) || !aligned(ids, 4)) return TFD_ERR_INVALID;
   if (id_map && !aligned(id_map, 4)) return TFD_ERR_INVALID;
   if (ws && !aligned(ws, 16)) return TFD_ERR_INVALID;
-  return tfd_internal::topk_launch(logits, rows, n, ld, k, id_map, vals, ids, k, nullptr, ws,
-                                   ws_bytes,
-                                   tfd_host::as_stream(stream));
+  return tfd_internal::topk_launch(logits, rows, n, ld, k, id_map, vals, ids, k, nullptr,
+                                   nullptr, 0, ws, ws_bytes, tfd_host::as_stream(stream));
 }

@@ -430,3 +430,54 @@ def test_full_fp8_head_top64(full_head, mode, rows):
     assert np.array_equal(ti.cpu().numpy(), oi) and same_bits(np32(tv), ov)
     assert np.array_equal(ti2.cpu().numpy(), oi) and same_bits(np32(tv2), ov)
     assert_topk_valid(np32(tv), ti.cpu().numpy(), acc, S, 64, what="fp8 top-64")
+
+
+@pytest.mark.parametrize("parts,k", [(64, 64), (65, 64), (300, 100), (1000, 512), (64, 100)])
+def test_fused_topk_threshold_from_part_maxima(parts, k):
+    """With k <= parts the fused top-k takes its threshold from the k-th largest part maximum (one
+    block per row); otherwise from the sub-group maxima (a cluster per row). Either way the result
+    is the exact top-k of the call's own logits."""
+    need_gpu()
+    case = make_case(40960, 1024, 9, tfd.W_BF16, tid=390, tie_frac=0.01)
+    y, tv, ti = tfd.tfd_head_gemv(case["w"], tfd.W_BF16, None, case["x"], tfd.OUT_F32, topk=k,
+                                  parts=parts)
+    torch.cuda.synchronize()
+    ov, oi = oracle_topk(np32(y), k)
+    assert np.array_equal(ti.cpu().numpy(), oi) and same_bits(np32(tv), ov)
+
+
+def test_fused_topk_of_all_equal_logits_falls_back_to_the_exact_select():
+    """Zero weights give a row of equal logits: every logit reaches the threshold, the candidate
+    list overflows, and the exact select over the row must still give the k lowest ids."""
+    need_gpu()
+    w = torch.zeros((65536, 256), dtype=torch.bfloat16, device="cuda")
+    x = inputs.normal_bf16((3, 256), 1.0, 395).cuda()
+    _, tv, ti = tfd.tfd_head_gemv(w, tfd.W_BF16, None, x, tfd.OUT_NONE, topk=64)
+    torch.cuda.synchronize()
+    assert np.array_equal(ti.cpu().numpy(), np.tile(np.arange(64, dtype=np.int32), (3, 1)))
+    assert np.all(np32(tv) == 0.0)
+
+
+@pytest.mark.parametrize("wfmt,rows,topk", [(tfd.W_BF16, 1, 1), (tfd.W_FP8_ROW, 16, 64),
+                                            (tfd.W_FP8_BLOCK32, 9, 8), (tfd.W_BF16, 12, 0)])
+def test_group_queue_repeats_bit_for_bit_and_leaves_the_counters_zero(wfmt, rows, topk):
+    """Calls with a workspace take 64-row groups from a queue shared by the blocks, so which block
+    computes a group changes from call to call: logits and top-k must still repeat bit for bit,
+    and each call must leave the workspace's counters at zero for the next."""
+    need_gpu()
+    case = make_case(65536, 4096, rows, wfmt, tid=397, tie_frac=0.01)
+    ws = tfd.zeroed_workspace(max(256, tfd.tfd_head_gemv_workspace(rows, 65536, topk)))
+    outs = []
+    for _ in range(3):
+        y, tv, ti = tfd.tfd_head_gemv(case["w"], wfmt, case["scales"], case["x"], tfd.OUT_F32,
+                                      topk=topk, ws=ws)
+        torch.cuda.synchronize()
+        assert torch.all(ws[:256] == 0), "counters left non-zero"
+        outs.append((np32(y), None if ti is None else (np32(tv), ti.cpu().numpy())))
+    for y, t in outs[1:]:
+        assert same_bits(y, outs[0][0])
+        if t is not None:
+            assert same_bits(t[0], outs[0][1][0]) and np.array_equal(t[1], outs[0][1][1])
+    if topk:
+        ov, oi = oracle_topk(outs[0][0], topk)
+        assert np.array_equal(outs[0][1][1], oi) and same_bits(outs[0][1][0], ov)

@@ -662,36 +662,67 @@ def measure_rows_of_path(wd, stream, peak):
     return out
 
 
-def run_fp8_case(args):
-    """A small case for profiling: the FP8 head with fused top-64 (no logits) at rows 1/5/10/15/16,
-    warmup + steps calls of each, one JSON line of us per call."""
+def run_head_case(args):
+    """A small case for profiling: the head in one format (--head bf16|row|block32|block32il; the
+    FP8 forms by default with fused top-64 and no logits, bf16 with fp32 logits and top-1, as the
+    headline) at rows 1/5/10/15/16 or --rows, warmup + steps calls of each (the steps from CUDA
+    graph replays), one JSON line of us per call."""
     import torch
 
     from speculative_decoding_draft_row_gb300 import tfd
     from synth import inputs
 
     torch.cuda.set_device(0)
-    stream = torch.cuda.current_stream()
-    mode = {"row": tfd.W_FP8_ROW, "block32": tfd.W_FP8_BLOCK32,
-            "block32il": tfd.W_FP8_BLOCK32_IL}[args.fp8]
+    fmt = args.head or args.fp8
+    mode = {"bf16": tfd.W_BF16, "row": tfd.W_FP8_ROW, "block32": tfd.W_FP8_BLOCK32,
+            "block32il": tfd.W_FP8_BLOCK32_IL}[fmt]
+    topk = args.topk if args.topk is not None else (1 if mode == tfd.W_BF16 else 64)
+    out_mode = tfd.OUT_F32 if mode == tfd.W_BF16 else tfd.OUT_NONE
     w, _ = inputs.head(tie_frac=0.01)
-    codes, scales = tfd.tfd_quant_fp8(w.cuda(), mode)
-    row_counts = ROWS_SWEEP if args.rows is None else [args.rows]
+    if mode == tfd.W_BF16:
+        codes, scales = w.cuda(), None
+    else:
+        codes, scales = tfd.tfd_quant_fp8(w.cuda(), mode)
+    del w
+    row_counts = (ROWS_SWEEP if args.rows is None
+                  else [1, 4, 8, 9, 12, 16] if args.rows == 0 else [args.rows])
     xs = {r: inputs.rows(32)[:r].cuda() for r in row_counts}
-    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(32, VOCAB, 64))
+    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(32, VOCAB, max(topk, 1)))
     out = {}
     for r in row_counts:
-        v = torch.empty((r, 64), dtype=torch.float32, device="cuda")
-        i = torch.empty((r, 64), dtype=torch.int32, device="cuda")
-        f = lambda: tfd.tfd_head_gemv(codes, mode, scales, xs[r], tfd.OUT_NONE, topk=64,
-                                      top_vals=v, top_ids=i, ws=ws, act_e4m3=args.w8a8)
+        y = torch.empty((r, VOCAB), dtype=torch.float32, device="cuda") if out_mode else None
+        v = torch.empty((r, max(topk, 1)), dtype=torch.float32, device="cuda")
+        i = torch.empty((r, max(topk, 1)), dtype=torch.int32, device="cuda")
+        f = lambda: tfd.tfd_head_gemv(codes, mode, scales, xs[r], out_mode, y=y, topk=topk,
+                                      top_vals=v if topk else None, top_ids=i if topk else None,
+                                      ws=ws, act_e4m3=args.w8a8)
         for _ in range(args.warmup):
             f()
         ms = time_graph(f, args.steps)
-        out[str(r)] = {"us": round(ms * 1e3, 2),
-                       "gbs": round(fp8_call_bytes(r) / (ms * 1e-3) / 1e9, 1)}
-    print(json.dumps({"case": f"fp8 {args.fp8}{' w8a8' if args.w8a8 else ''} top-64",
-                      "per_rows": out}), flush=True)
+        nb = (bf16_call_bytes(r) if mode == tfd.W_BF16 else fp8_call_bytes(r, max(topk, 1)))
+        out[str(r)] = {"us": round(ms * 1e3, 2), "gbs": round(nb / (ms * 1e-3) / 1e9, 1)}
+    print(json.dumps({"case": f"{fmt}{' w8a8' if args.w8a8 else ''} top-{topk}",
+                      "lib": os.environ.get("TFD_LIBRARY", "default"), "per_rows": out}),
+          flush=True)
+
+
+def run_ffma_compare(args):
+    """The bf16 head (fp32 logits + top-1) at rows 1/4/8/9/12/16 with the tensor-core MMA step
+    (the default build) and with the CUDA-core FFMA step of a -DTFD_GEMV_FFMA=1 build (built on
+    first use into _build/ffma; its two-n-tile ring is 4 steps deep to keep it from spilling)."""
+    from speculative_decoding_draft_row_gb300 import build
+    lib = build.build_library(extra_flags=["-DTFD_GEMV_FFMA=1", "-DTFD_GEMV_DEPTH_NT2=4"],
+                              build_dir=os.path.join(build.BUILD_DIR, "ffma"))
+    res = {}
+    for name, env in (("mma", {}), ("ffma", {"TFD_LIBRARY": lib})):
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--head", "bf16", "--rows",
+                            "0", "--steps", str(args.steps), "--warmup", str(args.warmup)],
+                           env=dict(os.environ, **env), cwd=ROOT, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(r.stderr[-2000:])
+        res[name] = json.loads(r.stdout.strip().splitlines()[-1])["per_rows"]
+    print(json.dumps({"case": "bf16 head, fp32 logits + top-1: MMA vs FFMA step", "ffma_lib": lib,
+                      **res}), flush=True)
 
 
 def run_case(args):
@@ -712,6 +743,29 @@ def run_case(args):
         out = torch.empty((PASS_STREAMS, PASS_HEADS * PASS_DIM), dtype=torch.bfloat16,
                           device="cuda")
         fn = lambda: tfd.tfd_window_attn(q, k, v, pos, krd, vrd, PASS_WINDOW, out=out)
+    elif c in ("pass", "passfp8"):
+        # one 5-step x 4-stream draft pass (bf16 head, or interleaved block-32 FP8 head), eager
+        from speculative_decoding_draft_row_gb300.draft_pass import DraftPass
+        w, _ = inputs.head(tie_frac=0.01)
+        wd = w.cuda()
+        del w
+        wo_c, wo_s = tfd.tfd_quant_fp8(inputs.linear(HIDDEN, HIDDEN, 40).cuda(), tfd.W_FP8_ROW)
+        w2_c, w2_s = tfd.tfd_quant_fp8(inputs.linear(HIDDEN, HIDDEN_FFN, 41).cuda(), tfd.W_FP8_ROW)
+        kr, vr = inputs.rings(PASS_STREAMS, PASS_RING, PASS_HEADS, PASS_DIM)
+        qkv = [inputs.pass_step_qkv(t, PASS_STREAMS, PASS_HEADS, PASS_DIM) for t in range(PASS_STEPS)]
+        us = [inputs.normal_bf16((PASS_STREAMS, HIDDEN_FFN), 1.0, 50 + t) for t in range(PASS_STEPS)]
+        if c == "pass":
+            head, fmt, sc = wd, tfd.W_BF16, None
+        else:
+            hc, sc = tfd.tfd_quant_fp8(wd, tfd.W_FP8_BLOCK32_IL)
+            head, fmt = hc, tfd.W_FP8_BLOCK32_IL
+            del wd
+        dp = DraftPass(wo_c, wo_s, w2_c, w2_s, head, fmt, sc, kr.cuda(), vr.cuda(), PASS_WINDOW,
+                       PASS_STEPS)
+        dp.load([q for q, _, _ in qkv], [k for _, k, _ in qkv], [v for _, _, v in qkv], us,
+                [511] * PASS_STREAMS, inputs.normal_bf16((PASS_STREAMS, HIDDEN), 1.0, 60).cuda(),
+                [5] * PASS_STREAMS, torch.zeros((PASS_STREAMS, PASS_STEPS), dtype=torch.int32))
+        fn = dp.enqueue
     elif c in ("rows17", "rows24", "rows32"):
         # a 17-32-row decode window on the full bf16 head: fp32 logits + fused top-1
         r = int(c[4:])
@@ -828,11 +882,13 @@ def run_trace(args):
     t = t[used]
     t0 = t[:, 0].min()
     med = lambda v: float(statistics.median(v.tolist())) if len(v) else None
-    groups = [(t[b, 2:59][t[b, 2:59] > 0] - t[b, 1]) for b in range(len(t))]
+    groups = [(t[b, 2:57][t[b, 2:57] > 0] - t[b, 1]) for b in range(len(t))]
     per_group = [float((g[-1] - 0) / len(g)) for g in groups if len(g)]
     out = {"case": f"{fmt} rows {rows} topk {topk}", "blocks": int(used.sum()),
            "entry_skew_ns": float(t[:, 0].max() - t0),
            "staging_ns_median": med(t[:, 1] - t[:, 0]), "staging_ns_max": float((t[:, 1] - t[:, 0]).max()),
+           "staging_phases_ns_median": ([med(t[:, 57] - t[:, 0]), med(t[:, 58] - t[:, 0]),
+                                         med(t[:, 59] - t[:, 0])] if (t[:, 57] > 0).all() else None),
            "first_group_ns_median": med(t[:, 2] - t[:, 1]),
            "group_ns_median": med(np.array(per_group)),
            "groups_per_block": [int(min(len(g) for g in groups)), int(max(len(g) for g in groups))],
@@ -882,12 +938,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", choices=["row", "block32", "block32il"], default=None,
                     help="profiling case: only the FP8 head with fused top-64")
-    ap.add_argument("--rows", type=int, default=None, choices=list(range(1, 33)),
-                    help="with --fp8: one row count instead of 1/5/10/15/16")
+    ap.add_argument("--head", choices=["bf16", "row", "block32", "block32il"], default=None,
+                    help="profiling case: one head format alone (see --rows, --topk, --w8a8)")
+    ap.add_argument("--rows", type=int, default=None, choices=list(range(0, 33)),
+                    help="with --head/--fp8: one row count instead of 1/5/10/15/16 (0: "
+                         "1/4/8/9/12/16)")
+    ap.add_argument("--topk", type=int, default=None,
+                    help="with --head/--fp8: the fused top-k (default 64 for FP8, 1 for bf16)")
+    ap.add_argument("--compare-ffma", action="store_true",
+                    help="the bf16 head with the MMA step and with the CUDA-core FFMA step")
     ap.add_argument("--w8a8", action="store_true",
-                    help="with --fp8: quantise the activation rows to E4M3 in the call")
+                    help="with --head/--fp8: quantise the activation rows to E4M3 in the call")
     ap.add_argument("--case", choices=["attn", "rescore", "topk64", "topk512", "twostage",
-                                       "rows17", "rows24", "rows32"],
+                                       "rows17", "rows24", "rows32", "pass", "passfp8"],
                     default=None,
                     help="profiling case: one row of the path alone")
     ap.add_argument("--trace", default=None, metavar="FMT:ROWS:TOPK",
@@ -903,8 +966,10 @@ def main():
         run_trace(args)
     elif args.impl == "reference":
         run_reference(args)
-    elif args.fp8:
-        run_fp8_case(args)
+    elif args.compare_ffma:
+        run_ffma_compare(args)
+    elif args.fp8 or args.head:
+        run_head_case(args)
     elif args.case:
         run_case(args)
     else:

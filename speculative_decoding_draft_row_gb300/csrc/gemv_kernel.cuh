@@ -335,8 +335,9 @@ gemv_kernel(const GemvArgs a) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int mt = warp % MT, ks = warp / MT;
-  // trace slots: 0 entry, 1 activations staged, 2 + j end of the block's group j (up to 57),
-  // 60 the SM, 61 groups done, 62 part keys written, 63 the join done (last block)
+  // trace slots: 0 entry, 1 activations staged, 2 + j end of the block's group j (up to 55),
+  // 57/58/59 the 4096-wide staging's loads landed / row scales known / converted, 60 the SM,
+  // 61 groups done, 62 part keys written, 63 the join done (last block)
   TFD_STAMP(a.trace, 0);
 #if TFD_TRACE
   if (a.trace != nullptr && tid == 0) {
@@ -694,6 +695,15 @@ gemv_kernel(const GemvArgs a) {
                                                         (int64_t)r * a.ldx + k0)
                       : make_uint4(0u, 0u, 0u, 0u);
     l2_prefetch();
+#if TFD_TRACE
+    if (a.trace != nullptr && tid == 0) {  // slot 56: a value of the loads, so slot 57 waits for them
+      uint32_t z = 0u;
+#pragma unroll
+      for (int r = 0; r < 8 * NT; ++r) z ^= v[r].x;
+      a.trace[(int64_t)blockIdx.x * kTraceSlots + 56] = z;
+    }
+#endif
+    TFD_STAMP(a.trace, 57);
     if (F16) {
       // each row's max |x| (non-negative floats order like their bit patterns): a warp maximum,
       // one shared atomic per warp and row
@@ -712,6 +722,7 @@ gemv_kernel(const GemvArgs a) {
       }
       __syncthreads();
       row_scales_from_max();
+      TFD_STAMP(a.trace, 58);
       // scaled by the row's 2^-e into f16 (exact for every bf16 down to 2^-32 of the row's max)
 #pragma unroll
       for (int r = 0; r < 8 * NT; ++r) {
@@ -727,6 +738,7 @@ gemv_kernel(const GemvArgs a) {
         v[r] = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
+    TFD_STAMP(a.trace, 59);
 #pragma unroll
     for (int r = 0; r < 8 * NT; ++r) xs[((s * NT + (r >> 3)) * H + hf) * 32 + (r & 7) * 4 + tt] = v[r];
   } else
@@ -1172,7 +1184,7 @@ gemv_kernel(const GemvArgs a) {
     }
     }
     rb ^= 1;
-    TFD_STAMP(a.trace, 2 + (j < 57 ? j : 57));
+    TFD_STAMP(a.trace, 2 + (j < 55 ? j : 55));
   };
   if constexpr (FASTK) {
     for (int j = 0;; ++j) {

@@ -98,3 +98,30 @@ def test_ring_write_and_window_positions():
     kr_b[0, 2] += 5.0
     out_b, _, _ = window_attn(q, k, v, [p], kr_b, vr, window=4)
     assert np.array_equal(out_a, out_b)
+
+
+def test_unrounded_terms_round_to_the_outputs_and_hold_their_invariants():
+    """The oracle's values before rounding (used to hold the GPU's bf16 outputs to their
+    rounding): they round to the oracle's own outputs; RoPE keeps every pair's magnitude, so the
+    exact key's pairs have the magnitudes reported for the normalised key; the softmax-weighted
+    magnitudes bound the output; with a given current key the output is attention over it."""
+    from oracle.numerics import round_bf16
+    S, H, D, ring = 2, 3, 128, 8
+    q, k, v = rand((S, H, D), 170), rand((S, H, D), 171), rand((S, H, D), 172)
+    kr, vr = rand((S, ring, H, D), 173), rand((S, ring, H, D), 174)
+    pos = [9, 40000]
+    terms = {}
+    out, kr2, _ = window_attn(q, k, v, pos, kr, vr, 5, terms=terms)
+    assert np.array_equal(round_bf16(terms["out_exact"]), out)
+    for s in range(S):
+        assert np.array_equal(round_bf16(terms["k_exact"][s]), kr2[s, pos[s] % ring])
+    ke = terms["k_exact"]
+    assert np.allclose(np.hypot(ke[..., :64], ke[..., 64:]), terms["k_pair"][..., :64], rtol=1e-12)
+    assert (terms["abs_out"] >= np.abs(terms["out_exact"]) * (1 - 1e-12)).all()
+    assert (terms["abs_dev"] <= 2 * terms["abs_out"] + 1e-12).all()
+    # the current key given: its values are the ones attended
+    kc = round_bf16(ke) + 0.25
+    out_c, kr3, _ = window_attn(q, k, v, pos, kr, vr, 5, k_cur=kc)
+    for s in range(S):
+        assert np.array_equal(kr3[s, pos[s] % ring], kc[s])
+    assert not np.array_equal(out_c, out)

@@ -99,3 +99,24 @@ def test_absorb_of_a_span_equals_absorbs_of_its_pieces():
     a = absorb(k[:, :2], v[:, :2], [30], kr, vr)
     b = absorb(k[:, 2:], v[:, 2:], [32], *a)
     assert np.array_equal(whole[0], b[0]) and np.array_equal(whole[1], b[1])
+
+
+def test_unrounded_rmsnorm_and_absorb_terms():
+    """rmsnorm_rows(exact=True) rounds to rmsnorm_rows; the absorb's exact keys round to the keys
+    it writes and keep each rotation pair's magnitude; unwritten slots are NaN in the terms."""
+    from oracle.attn import rmsnorm, rope
+    x = bf((3, 256), 3.0, 180)
+    ex = rmsnorm_rows(x, None, 1e-6, exact=True)
+    assert np.array_equal(round_bf16(ex), rmsnorm_rows(x, None, 1e-6))
+    S, n, H, D, ring = 1, 3, 2, 128, 8
+    k, v = bf((S, n, H, D), 1.0, 181), bf((S, n, H, D), 1.0, 182)
+    kr, vr = bf((S, ring, H, D), 1.0, 183), bf((S, ring, H, D), 1.0, 184)
+    terms = {}
+    okr, _ = absorb(k, v, [6], kr, vr, terms=terms)
+    written = ~np.isnan(terms["k_exact"][..., 0])
+    assert written.sum() == n * H and written[0, [6, 7, 0]].all()
+    w = ~np.isnan(terms["k_exact"])
+    assert np.array_equal(round_bf16(terms["k_exact"][w]), okr[w])
+    ke, kp = terms["k_exact"][0, 6, 0], terms["k_pair"][0, 6, 0]
+    assert np.allclose(np.hypot(ke[:64], ke[64:]), kp[:64], rtol=1e-12)
+    assert np.allclose(ke, rope(rmsnorm(k[0, 0, 0], np.ones(D), 1e-6), 6, 10000.0), rtol=0, atol=0)

@@ -678,7 +678,12 @@ def run_head_case(args):
             "block32il": tfd.W_FP8_BLOCK32_IL}[fmt]
     topk = args.topk if args.topk is not None else (1 if mode == tfd.W_BF16 else 64)
     out_mode = tfd.OUT_F32 if mode == tfd.W_BF16 else tfd.OUT_NONE
-    w, _ = inputs.head(tie_frac=0.01)
+    if args.shape:  # another matrix than the head: N x K ~ N(0, 0.02)
+        n_out, k_in = (int(v) for v in args.shape.split(":"))
+        w = inputs.linear(n_out, k_in, 40)
+    else:
+        w, _ = inputs.head(tie_frac=0.01)
+    n_out, k_in = w.shape
     if mode == tfd.W_BF16:
         codes, scales = w.cuda(), None
     else:
@@ -686,11 +691,11 @@ def run_head_case(args):
     del w
     row_counts = (ROWS_SWEEP if args.rows is None
                   else [1, 4, 8, 9, 12, 16] if args.rows == 0 else [args.rows])
-    xs = {r: inputs.rows(32)[:r].cuda() for r in row_counts}
-    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(32, VOCAB, max(topk, 1)))
+    xs = {r: inputs.rows(32, hidden=k_in)[:r].cuda() for r in row_counts}
+    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(32, n_out, max(topk, 1)))
     out = {}
     for r in row_counts:
-        y = torch.empty((r, VOCAB), dtype=torch.float32, device="cuda") if out_mode else None
+        y = torch.empty((r, n_out), dtype=torch.float32, device="cuda") if out_mode else None
         v = torch.empty((r, max(topk, 1)), dtype=torch.float32, device="cuda")
         i = torch.empty((r, max(topk, 1)), dtype=torch.int32, device="cuda")
         f = lambda: tfd.tfd_head_gemv(codes, mode, scales, xs[r], out_mode, y=y, topk=topk,
@@ -700,6 +705,8 @@ def run_head_case(args):
             f()
         ms = time_graph(f, args.steps)
         nb = (bf16_call_bytes(r) if mode == tfd.W_BF16 else fp8_call_bytes(r, max(topk, 1)))
+        if args.shape:
+            nb = n_out * k_in * (2 if mode == tfd.W_BF16 else 1) + r * k_in * 2
         out[str(r)] = {"us": round(ms * 1e3, 2), "gbs": round(nb / (ms * 1e-3) / 1e9, 1)}
     print(json.dumps({"case": f"{fmt}{' w8a8' if args.w8a8 else ''} top-{topk}",
                       "lib": os.environ.get("TFD_LIBRARY", "default"), "per_rows": out}),
@@ -852,11 +859,15 @@ def run_trace(args):
     from synth import inputs
 
     torch.cuda.set_device(0)
-    fmt, rows, topk = args.trace.split(":")
-    rows, topk = int(rows), int(topk)
+    spec = args.trace.split(":")
+    fmt, rows, topk = spec[0], int(spec[1]), int(spec[2])
     mode = {"bf16": tfd.W_BF16, "row": tfd.W_FP8_ROW, "block32": tfd.W_FP8_BLOCK32,
             "block32il": tfd.W_FP8_BLOCK32_IL}[fmt]
-    w, _ = inputs.head(tie_frac=0.01)
+    if len(spec) == 5:  # another matrix: N x K ~ N(0, 0.02)
+        w = inputs.linear(int(spec[3]), int(spec[4]), 40)
+    else:
+        w, _ = inputs.head(tie_frac=0.01)
+    n_out, k_in = w.shape
     wd = w.cuda()
     del w
     if mode == tfd.W_BF16:
@@ -864,12 +875,13 @@ def run_trace(args):
     else:
         codes, scales = tfd.tfd_quant_fp8(wd, mode)
         del wd
-    x = inputs.rows(32)[:rows].cuda()
-    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(rows, VOCAB, max(topk, 1)))
+    x = inputs.rows(32, hidden=k_in)[:rows].cuda()
+    ws = tfd.zeroed_workspace(tfd.tfd_head_gemv_workspace(rows, n_out, max(topk, 1)))
     buf = torch.zeros((1024, 64), dtype=torch.int64, device="cuda")
     lib = tfd.library()
     lib.tfd_trace_set.argtypes = [ctypes.c_void_p]
-    f = lambda: tfd.tfd_head_gemv(codes, mode, scales, x, tfd.OUT_NONE, topk=topk, ws=ws)
+    f = lambda: tfd.tfd_head_gemv(codes, mode, scales, x, tfd.OUT_NONE, topk=topk,
+                                  ws=ws if topk else None)
     for _ in range(args.warmup):
         f()
     torch.cuda.synchronize()
@@ -884,11 +896,13 @@ def run_trace(args):
     med = lambda v: float(statistics.median(v.tolist())) if len(v) else None
     groups = [(t[b, 2:57][t[b, 2:57] > 0] - t[b, 1]) for b in range(len(t))]
     per_group = [float((g[-1] - 0) / len(g)) for g in groups if len(g)]
-    out = {"case": f"{fmt} rows {rows} topk {topk}", "blocks": int(used.sum()),
+    gpu_ms = time_graph(f, 40)
+    out = {"case": f"{fmt} {n_out}x{k_in} rows {rows} topk {topk}", "blocks": int(used.sum()),
+           "graph_us": round(gpu_ms * 1e3, 2),
            "entry_skew_ns": float(t[:, 0].max() - t0),
            "staging_ns_median": med(t[:, 1] - t[:, 0]), "staging_ns_max": float((t[:, 1] - t[:, 0]).max()),
-           "staging_phases_ns_median": ([med(t[:, 57] - t[:, 0]), med(t[:, 58] - t[:, 0]),
-                                         med(t[:, 59] - t[:, 0])] if (t[:, 57] > 0).all() else None),
+           "staging_phases_ns_median": [med(t[:, q][t[:, q] > 0] - t[:, 0][t[:, q] > 0])
+                                        if (t[:, q] > 0).any() else None for q in (57, 58, 59)],
            "first_group_ns_median": med(t[:, 2] - t[:, 1]),
            "group_ns_median": med(np.array(per_group)),
            "groups_per_block": [int(min(len(g) for g in groups)), int(max(len(g) for g in groups))],
@@ -945,6 +959,8 @@ def main():
                          "1/4/8/9/12/16)")
     ap.add_argument("--topk", type=int, default=None,
                     help="with --head/--fp8: the fused top-k (default 64 for FP8, 1 for bf16)")
+    ap.add_argument("--shape", default=None, metavar="N:K",
+                    help="with --head: an N x K matrix ~ N(0, 0.02) instead of the head")
     ap.add_argument("--compare-ffma", action="store_true",
                     help="the bf16 head with the MMA step and with the CUDA-core FFMA step")
     ap.add_argument("--w8a8", action="store_true",
@@ -953,9 +969,10 @@ def main():
                                        "rows17", "rows24", "rows32", "pass", "passfp8"],
                     default=None,
                     help="profiling case: one row of the path alone")
-    ap.add_argument("--trace", default=None, metavar="FMT:ROWS:TOPK",
+    ap.add_argument("--trace", default=None, metavar="FMT:ROWS:TOPK[:N:K]",
                     help="phase stamps of one head GEMV call from a -DTFD_TRACE=1 build, e.g. "
-                         "row:16:64 (FMT bf16, row, block32 or block32il)")
+                         "row:16:64 (FMT bf16, row, block32 or block32il; N:K another matrix "
+                         "than the head)")
     ap.add_argument("--no-extras", action="store_true",
                     help="time the headline calls only (no e2e, FP8 or CPU baseline): a small "
                          "case for profiling")

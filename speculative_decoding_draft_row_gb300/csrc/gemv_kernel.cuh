@@ -336,7 +336,8 @@ gemv_kernel(const GemvArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int mt = warp % MT, ks = warp / MT;
   // trace slots: 0 entry, 1 activations staged, 2 + j end of the block's group j (up to 55),
-  // 57/58/59 the 4096-wide staging's loads landed / row scales known / converted, 60 the SM,
+  // 57/58/59 the 4096-wide staging's loads landed / row scales known / converted (general staging:
+  // first barrier passed / chunks stored / converted), 60 the SM,
   // 61 groups done, 62 part keys written, 63 the join done (last block)
   TFD_STAMP(a.trace, 0);
 #if TFD_TRACE
@@ -350,7 +351,7 @@ gemv_kernel(const GemvArgs a) {
   // 4 crank .. 4 crank + 3 of every group of the cluster; the leader (crank 0) sums the blocks'
   // partials in rank order and runs the epilogue.
   namespace cg = cooperative_groups;
-  const int csplit = KSL == 1 ? 1 : a.csplit;
+  const int csplit = (KSL == 1 || VAR >= 1) ? 1 : a.csplit;  // VAR >= 1: chosen without a split
   const int crank = csplit > 1 ? (int)cg::this_cluster().block_rank() : 0;
   const int cid = blockIdx.x / csplit;
   const int kstep0 = crank * KSL * ssl;  // first step of this block's k range
@@ -556,14 +557,25 @@ gemv_kernel(const GemvArgs a) {
     }
   };
   // The ring's first steps are issued before the activations are staged, except where the staging
-  // keeps every row's chunk in registers (the 4096-wide form): there the L2 prefetch below covers
-  // the staging, and the ring follows it.
+  // keeps every row's chunk in registers (the 4096-wide form) and in a cluster split (small
+  // matrices, whose staging is most of the call): there the activation loads go first, the L2
+  // prefetch below covers the staging, and the ring follows it.
   constexpr bool PRIME_LATE = VAR >= 1 && XF == TFD_X_BF16 && !AQ && NT <= 2;
-  if constexpr (!PRIME_LATE) prime();
+  if (!PRIME_LATE && csplit == 1) prime();
   // Staging the activations takes longer than the ring's loads (every block reads all rows, which
   // all blocks want at once); meanwhile the first TFD_GEMV_PREFETCH bytes of the block's first
   // group are fetched into L2, so the weight stream does not pause.
   auto l2_prefetch = [&]() {
+  if (csplit > 1 && g_begin < g_end && tid < GR) {
+    // this block's k range of each row of its first group, a row a thread
+    const int64_t row = row_off + g_begin * GR + tid;
+    const int64_t kb = (int64_t)kstep0 * STEPK;
+    const int64_t kl = (int64_t)KSL * ssl * STEPK < K - kb ? (int64_t)KSL * ssl * STEPK : K - kb;
+    if (row < N && kl > 0)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(wbase + row * row_bytes + kb * EB),
+                   "r"((uint32_t)(kl * EB))
+                   : "memory");
+  }
   if (csplit == 1 && g_begin < g_end && tid < kPrefetchParts) {
     const int64_t row0 = row_off + g_begin * GR;
     const int64_t gbytes = (N - row0 < GR ? N - row0 : GR) * row_bytes;
@@ -577,8 +589,11 @@ gemv_kernel(const GemvArgs a) {
                    : "memory");
   }
   };
-  // (the 4096-wide staging issues its activation loads first, so they are not queued behind this)
-  if constexpr (VAR == 0 || !(XF == TFD_X_BF16 && !AQ && NT <= 2)) l2_prefetch();
+  // (the 4096-wide staging and a cluster split's staging issue their activation loads first, so
+  // they are not queued behind this)
+  if constexpr (VAR == 0 || !(XF == TFD_X_BF16 && !AQ && NT <= 2)) {
+    if (csplit == 1) l2_prefetch();
+  }
 
   for (int i = tid; i < MT * kMaxRowsPad; i += kThreads) sbest[i] = 0ull;
   if (tid < kMaxRowsPad) { sxmax[tid] = 0u; spmax[tid] = 0u; }
@@ -588,15 +603,18 @@ gemv_kernel(const GemvArgs a) {
   }
   __syncthreads();
   // bf16 activations for FP8 weights: the raw rows are staged in one pass that also takes each
-  // row's max |x|; the power-of-two scaling into f16 is applied afterwards in shared memory. A
-  // block that stages only part of k (cluster split) takes the max over the whole row first.
+  // row's max |x|; the power-of-two scaling into f16 is applied afterwards in shared memory.
   constexpr bool ONEPASS_C = F16 && XF == TFD_X_BF16 && !AQ;
   // 4096-wide bf16 activations staged whole by one block: 512 chunks of 8 a row, one per thread,
   // so thread tid owns k = 8 tid .. 8 tid + 7 of every row (constant geometry, every row's load in
   // flight at once, conversions in registers)
   constexpr bool STAGE4K_C = VAR >= 1 && XF == TFD_X_BF16 && !AQ && NT <= 2 && kThreads * 8 == 4096;
   constexpr bool stage4k = STAGE4K_C;
-  const bool onepass = ONEPASS_C && csplit == 1 && !stage4k;
+  // (in a cluster split each block scales by the max over its own k range, and its partial sums
+  // are scaled back before the cluster sums them: power-of-two scalings are exact, so the logits
+  // are the same bits as with one scale for the whole row)
+  const bool onepass = ONEPASS_C && !stage4k;
+  if constexpr (!STAGE4K_C) TFD_STAMP(a.trace, 57);  // general staging: after the first barrier
   if (F16 && !onepass && !stage4k) {
     if (F16) {
       // per-row max |x| over the whole row (non-negative floats order like their bit patterns): the
@@ -742,123 +760,136 @@ gemv_kernel(const GemvArgs a) {
 #pragma unroll
     for (int r = 0; r < 8 * NT; ++r) xs[((s * NT + (r >> 3)) * H + hf) * 32 + (r & 7) * 4 + tt] = v[r];
   } else
-  // Chunk idx (8 consecutive k of one activation row) goes to one 16-byte fragment slot; XU chunks a
-  // thread are loaded before any is stored, and each block starts at its own offset, so the blocks
-  // do not all ask for the same lines of the activations at once.
+  // Chunk (r, c) (8 consecutive k of activation row r at column c of this block's k range) goes to
+  // one 16-byte fragment slot. Thread tid takes columns tid, tid + 512, ... (a block-uniform loop),
+  // so each column's place in the fragment order is computed once with compile-time divisions;
+  // XU rows of a column are loaded before any is stored; rows past `rows` only get zeros.
   {
-    const int chunks_per_row = spad * STEPK / 8;
-    const int total = 8 * NT * chunks_per_row;
-    const int rot = (int)(((int64_t)blockIdx.x * 2053) % total);
+    const int cpr = spad * STEPK / 8;  // chunks per row of this block's k range
+    constexpr int NR = 8 * NT;         // activation rows of the tile
     constexpr int XU = XF == TFD_X_F32 ? 4 : 8;
-    for (int base = 0; base < total; base += XU * kThreads) {  // the same trip count in every lane
-      uint4 raw[XU][XF == TFD_X_F32 ? 2 : 1];
-      int cidx[XU];
+    for (int c0 = 0; c0 < cpr; c0 += kThreads) {
+      const int c = c0 + tid;
+      const bool cin = c < cpr;
+      const int k0 = c * 8;  // within the block's k range
+      const int s = k0 / STEPK;
+      const int rem = k0 - s * STEPK;
+      // A thread's 16-element chunk is contiguous, except in the block-32 form, where it is 8
+      // elements of each 32-wide scale block of the step (so every MMA stays inside one block).
+      const int tt = BLK ? (rem & 31) >> 3 : rem / E;
+      const int hf = BLK ? rem >> 5 : (rem - tt * E) >> 3;
+      const int64_t kg = (int64_t)kstep0 * STEPK + k0;  // in the whole row
+      const bool kin = cin && kg < K;
 #pragma unroll
-      for (int u = 0; u < XU; ++u) {
-        int idx = base + u * kThreads + tid;
-        const bool in = idx < total;
-        idx += rot;
-        if (idx >= total) idx -= total;
-        cidx[u] = in ? idx : -1;
-        const int r = idx / chunks_per_row;
-        const int64_t kg = (int64_t)kstep0 * STEPK + (int64_t)(idx - r * chunks_per_row) * 8;
-        const bool ok = in && r < rows && kg < K;
-        if (XF == TFD_X_F32) {
-          const uint4* p = reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(a.x) +
-                                                          (int64_t)r * a.ldx + kg);
-          raw[u][0] = ok ? p[0] : make_uint4(0u, 0u, 0u, 0u);
-          raw[u][XF == TFD_X_F32 ? 1 : 0] = ok ? p[1] : make_uint4(0u, 0u, 0u, 0u);
-        } else {
-          raw[u][0] = ok ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
-                                                         (int64_t)r * a.ldx + kg)
-                         : make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
+      for (int r0 = 0; r0 < NR; r0 += XU) {
+        if (r0 >= rows) {  // block-uniform: padding rows are zeros
 #pragma unroll
-      for (int u = 0; u < XU; ++u) {
-        const int idx = cidx[u];
-        const int r = idx / chunks_per_row;
-        const int c = idx - r * chunks_per_row;
-        const int k0 = c * 8;  // within the block's k range
-        const int s = k0 / STEPK;
-        const int rem = k0 - s * STEPK;
-        // A thread's 16-element chunk is contiguous, except in the block-32 form, where it is 8
-        // elements of each 32-wide scale block of the step (so every MMA stays inside one block).
-        const int tt = BLK ? (rem & 31) >> 3 : rem / E;
-        const int hf = BLK ? rem >> 5 : (rem - tt * E) >> 3;
-        const int ln = (r & 7) * 4 + tt;
-        const int nt = r >> 3;
-        const uint4 v = raw[u][0];
-        if (ONEPASS_C && onepass) {  // block-uniform
-          // raw bf16 bits in the f16 slot; the row's max |x| (non-negative floats order like
-          // their bit patterns), one shared atomic per warp whose lanes share a row
-          uint32_t m = 0u;
-          const int rr = idx >= 0 ? r : -1;
-          if (idx >= 0) {
-            xs[((s * NT + nt) * H + hf) * 32 + ln] = v;
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          for (int u = 0; u < XU; ++u) {
+            const int r = r0 + u;
+            if (r >= NR || !cin) continue;
+            const int ln = (r & 7) * 4 + tt, nt = r >> 3;
+            if (AQ) reinterpret_cast<uint2*>(xs)[((s * NT + nt) * 32 + ln) * 2 + hf] = make_uint2(0u, 0u);
+            else
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              m = max(m, max((w[i] << 16) & 0x7FFFFFFFu, w[i] & 0x7FFF0000u));
-          }
-          const int r0 = __shfl_sync(0xffffffffu, rr, 0);
-          if (__all_sync(0xffffffffu, rr == r0)) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0 && r0 >= 0 && m != 0u) atomicMax(&sxmax[r0], m);
-          } else if (rr >= 0 && m != 0u) {
-            atomicMax(&sxmax[rr], m);
+              for (int pl = 0; pl < PL; ++pl)
+                xs[(((pl * spad + s) * NT + nt) * H + hf) * 32 + ln] = make_uint4(0u, 0u, 0u, 0u);
           }
           continue;
         }
-        if (idx < 0) continue;
-        if (AQ) {
-          // 8 codes: code = e4m3(fl32(x / s)), s = 0 for a zero row (its codes are zero)
-          const float inv = __uint_as_float(sxmax[r]);
-          const uint32_t uw[4] = {v.x, v.y, v.z, v.w};
-          uint32_t q[4];
+        uint4 raw[XU][XF == TFD_X_F32 ? 2 : 1];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float lo = bf16_lo(uw[i]), hi = bf16_hi(uw[i]);
-            if (inv > 0.0f) { lo = __fdiv_rn(lo, inv); hi = __fdiv_rn(hi, inv); }
-            q[i] = f32x2_to_e4m3x2(lo, hi);
-          }
-          reinterpret_cast<uint2*>(xs)[((s * NT + nt) * 32 + ln) * 2 + hf] =
-              make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
-        } else if (XF == TFD_X_BF16 && !F16) {
-          xs[((s * NT + nt) * H + hf) * 32 + ln] = v;
-        } else {
-          const float inv = F16 ? __uint_as_float(sxmax[r]) : 1.0f;
-          float f[8];
-          if (XF == TFD_X_BF16) {
-            const uint32_t uw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) { f[2 * i] = bf16_lo(uw[i]); f[2 * i + 1] = bf16_hi(uw[i]); }
+        for (int u = 0; u < XU; ++u) {
+          const int r = r0 + u;
+          const bool ok = kin && r < rows && r < NR;
+          if (XF == TFD_X_F32) {
+            const uint4* p = reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(a.x) +
+                                                            (int64_t)r * a.ldx + kg);
+            raw[u][0] = ok ? p[0] : make_uint4(0u, 0u, 0u, 0u);
+            raw[u][XF == TFD_X_F32 ? 1 : 0] = ok ? p[1] : make_uint4(0u, 0u, 0u, 0u);
           } else {
-            const uint4 v2 = raw[u][XF == TFD_X_F32 ? 1 : 0];
-            f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
-            f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
-            f[4] = __uint_as_float(v2.x); f[5] = __uint_as_float(v2.y);
-            f[6] = __uint_as_float(v2.z); f[7] = __uint_as_float(v2.w);
+            raw[u][0] = ok ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.x) +
+                                                           (int64_t)r * a.ldx + kg)
+                           : make_uint4(0u, 0u, 0u, 0u);
           }
-          uint16_t h[3][8];
+        }
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            if (PL == 1) h[0][e] = f32_to_f16_bits(f[e] * inv);   // bf16 x, FP8 weights
-            else split3<F16>(f[e] * inv, h[0][e], h[1][e], h[2][e]);
+        for (int u = 0; u < XU; ++u) {
+          const int r = r0 + u;
+          if (r >= NR) continue;
+          const int ln = (r & 7) * 4 + tt;
+          const int nt = r >> 3;
+          const uint4 v = raw[u][0];
+          if (ONEPASS_C && onepass) {  // block-uniform
+            // raw bf16 bits in the f16 slot; the row's max |x| (non-negative floats order like
+            // their bit patterns): a warp maximum and one shared atomic per warp
+            uint32_t m = 0u;
+            if (cin) {
+              xs[((s * NT + nt) * H + hf) * 32 + ln] = v;
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                m = max(m, max((w[i] << 16) & 0x7FFFFFFFu, w[i] & 0x7FFF0000u));
+            }
+            if (r < rows) {  // block-uniform
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+              if (lane == 0 && m != 0u) atomicMax(&sxmax[r], m);
+            }
+            continue;
           }
+          if (!cin) continue;
+          if (AQ) {
+            // 8 codes: code = e4m3(fl32(x / s)), s = 0 for a zero row (its codes are zero)
+            const float inv = __uint_as_float(sxmax[r]);
+            const uint32_t uw[4] = {v.x, v.y, v.z, v.w};
+            uint32_t q[4];
 #pragma unroll
-          for (int pl = 0; pl < PL; ++pl) {
-            uint4 o;
-            o.x = h[pl][0] | ((uint32_t)h[pl][1] << 16);
-            o.y = h[pl][2] | ((uint32_t)h[pl][3] << 16);
-            o.z = h[pl][4] | ((uint32_t)h[pl][5] << 16);
-            o.w = h[pl][6] | ((uint32_t)h[pl][7] << 16);
-            xs[(((pl * spad + s) * NT + nt) * H + hf) * 32 + ln] = o;
+            for (int i = 0; i < 4; ++i) {
+              float lo = bf16_lo(uw[i]), hi = bf16_hi(uw[i]);
+              if (inv > 0.0f) { lo = __fdiv_rn(lo, inv); hi = __fdiv_rn(hi, inv); }
+              q[i] = f32x2_to_e4m3x2(lo, hi);
+            }
+            reinterpret_cast<uint2*>(xs)[((s * NT + nt) * 32 + ln) * 2 + hf] =
+                make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+          } else if (XF == TFD_X_BF16 && !F16) {
+            xs[((s * NT + nt) * H + hf) * 32 + ln] = v;
+          } else {
+            const float inv = F16 ? __uint_as_float(sxmax[r]) : 1.0f;
+            float f[8];
+            if (XF == TFD_X_BF16) {
+              const uint32_t uw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) { f[2 * i] = bf16_lo(uw[i]); f[2 * i + 1] = bf16_hi(uw[i]); }
+            } else {
+              const uint4 v2 = raw[u][XF == TFD_X_F32 ? 1 : 0];
+              f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+              f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+              f[4] = __uint_as_float(v2.x); f[5] = __uint_as_float(v2.y);
+              f[6] = __uint_as_float(v2.z); f[7] = __uint_as_float(v2.w);
+            }
+            uint16_t h[3][8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              if (PL == 1) h[0][e] = f32_to_f16_bits(f[e] * inv);   // bf16 x, FP8 weights
+              else split3<F16>(f[e] * inv, h[0][e], h[1][e], h[2][e]);
+            }
+#pragma unroll
+            for (int pl = 0; pl < PL; ++pl) {
+              uint4 o;
+              o.x = h[pl][0] | ((uint32_t)h[pl][1] << 16);
+              o.y = h[pl][2] | ((uint32_t)h[pl][3] << 16);
+              o.z = h[pl][4] | ((uint32_t)h[pl][5] << 16);
+              o.w = h[pl][6] | ((uint32_t)h[pl][7] << 16);
+              xs[(((pl * spad + s) * NT + nt) * H + hf) * 32 + ln] = o;
+            }
           }
         }
       }
     }
+    if constexpr (!STAGE4K_C) {
+      if (csplit > 1) l2_prefetch();
+    }
+    TFD_STAMP(a.trace, 58);  // this thread's chunks stored
     if (ONEPASS_C && onepass) {
       __syncthreads();  // every row's max |x| and every raw chunk is in shared memory
       row_scales_from_max();
@@ -869,20 +900,21 @@ gemv_kernel(const GemvArgs a) {
         const int ln = i & 31;
         const int nt = (i / (H * 32)) % NT;
         const int r = nt * 8 + (ln >> 2);
+        if (r >= rows) continue;  // padding rows hold zeros already
         const float inv = __uint_as_float(sxmax[r]);
         const uint4 v = xs[i];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          o[j] = (uint32_t)f32_to_f16_bits(bf16_lo(w[j]) * inv) |
-                 ((uint32_t)f32_to_f16_bits(bf16_hi(w[j]) * inv) << 16);
+          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o[j]) : "f"(bf16_hi(w[j]) * inv), "f"(bf16_lo(w[j]) * inv));
         xs[i] = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
+    TFD_STAMP(a.trace, 59);
   }
   __syncthreads();
-  if constexpr (PRIME_LATE) prime();
+  if (PRIME_LATE || csplit > 1) prime();
   TFD_STAMP(a.trace, 1);
 
   // One step: MMA j of the step takes elements [4j, 4j + 4) of each thread's chunk. All activation
@@ -1033,7 +1065,7 @@ gemv_kernel(const GemvArgs a) {
   // Returns the stored value (NaN outside the output).
   auto epi = [&](int64_t row, int act, float v, int slot, float rsc) -> float {
     if (row >= N || act >= rows) return __uint_as_float(0x7FC00000u);
-    if (F16) v *= sxscale[act];
+    if (F16 && !(ONEPASS_C && onepass && csplit > 1)) v *= sxscale[act];  // else scaled per block
     if (WF == TFD_W_FP8_ROW) v *= rsc;
     const int64_t yi = (int64_t)act * a.ldy + row;
     if (a.out_mode == TFD_OUT_F32) {
@@ -1168,7 +1200,14 @@ gemv_kernel(const GemvArgs a) {
         v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
       }
       if (csplit == 1) finish_tile(gi, mr, nr * 8 + 2 * t, v, 0);
-      else cpart[(rb * 4 * NT + warp) * 32 + lane] = v;
+      else {
+        if (ONEPASS_C && onepass) {  // this block's own activation scale, before the cluster sum
+          const int act0 = nr * 8 + 2 * t;
+          v.x *= sxscale[act0]; v.z *= sxscale[act0];
+          v.y *= sxscale[act0 + 1]; v.w *= sxscale[act0 + 1];
+        }
+        cpart[(rb * 4 * NT + warp) * 32 + lane] = v;
+      }
     }
     if (csplit > 1) {
       cg::this_cluster().sync();  // every block's partial of group gi is in its shared memory

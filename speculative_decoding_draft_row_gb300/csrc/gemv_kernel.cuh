@@ -297,11 +297,14 @@ struct Layout {
 
 // VAR: 0 the general form; 1 a 4096-wide matrix staged by one block (no cluster split) with bf16
 // activations: constant staging geometry; 2 that, plus the unrolled check-free weight loop (n a
-// multiple of the group rows). The host picks the instantiation.
+// multiple of the group rows); 3 the unrolled check-free weight loop of a 4096-wide matrix split
+// over a cluster of two (a small matrix, e.g. the attention output projection). The host picks
+// the instantiation.
 template <int WF, int XF, int NT, int D, int KSL, int VAR = 0>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? TFD_GEMV_MINB_NT1 : 1)
 gemv_kernel(const GemvArgs a) {
-  constexpr bool FASTP = VAR == 2;
+  constexpr bool FASTP = VAR >= 2;
+  constexpr int CSC = VAR == 3 ? 2 : 1;  // the cluster split the fast loop is built for
   using L = Layout<WF, XF, NT, KSL>;
   constexpr int MT = L::MT;
   constexpr int GR = 16 * MT;  // rows per group
@@ -347,11 +350,11 @@ gemv_kernel(const GemvArgs a) {
     a.trace[(int64_t)blockIdx.x * kTraceSlots + 60] = smid;
   }
 #endif
-  // Split k over a cluster (small vocabularies): block crank of cluster cid takes k-slices
-  // 4 crank .. 4 crank + 3 of every group of the cluster; the leader (crank 0) sums the blocks'
-  // partials in rank order and runs the epilogue.
+  // Split k over a cluster (small matrices, or 17-32 rows of a 4096-wide head): block crank of
+  // cluster cid takes k-slices 4 crank .. 4 crank + 3 of every group of the cluster; the leader
+  // (crank 0) sums the blocks' partials in rank order and runs the epilogue.
   namespace cg = cooperative_groups;
-  const int csplit = (KSL == 1 || VAR >= 1) ? 1 : a.csplit;  // VAR >= 1: chosen without a split
+  const int csplit = (KSL == 1 || VAR == 1 || VAR == 2) ? 1 : VAR == 3 ? 2 : a.csplit;
   const int crank = csplit > 1 ? (int)cg::this_cluster().block_rank() : 0;
   const int cid = blockIdx.x / csplit;
   const int kstep0 = crank * KSL * ssl;  // first step of this block's k range
@@ -506,10 +509,10 @@ gemv_kernel(const GemvArgs a) {
     if (++ld_s == ssl_loop) { ld_s = 0; ld_g = seq_group(++ld_j); set_group(); }
   };
 
-  // Fast path (the FASTP instantiation, chosen on the host): k == 4096, 4 k-slices, no cluster
-  // split, n a multiple of the group rows.
+  // Fast path (the FASTP instantiations, chosen on the host): k == 4096, 4 k-slices, no cluster
+  // split or a split of CSC blocks, n a multiple of the group rows.
   constexpr int FK = 4096;
-  constexpr int SSLC = FK / (KSL * STEPK);  // steps per k-slice at k == FK
+  constexpr int SSLC = FK / (KSL * STEPK * CSC);  // steps per k-slice at k == FK
   constexpr bool FASTK = FASTP && KSL == 4 && SSLC >= D;
   constexpr int64_t FROWB = (int64_t)FK * EB;
   const bool fast = FASTK && g_begin < g_end;
@@ -560,7 +563,7 @@ gemv_kernel(const GemvArgs a) {
   // keeps every row's chunk in registers (the 4096-wide form) and in a cluster split (small
   // matrices, whose staging is most of the call): there the activation loads go first, the L2
   // prefetch below covers the staging, and the ring follows it.
-  constexpr bool PRIME_LATE = VAR >= 1 && XF == TFD_X_BF16 && !AQ && NT <= 2;
+  constexpr bool PRIME_LATE = (VAR == 1 || VAR == 2) && XF == TFD_X_BF16 && !AQ && NT <= 2;
   if (!PRIME_LATE && csplit == 1) prime();
   // Staging the activations takes longer than the ring's loads (every block reads all rows, which
   // all blocks want at once); meanwhile the first TFD_GEMV_PREFETCH bytes of the block's first
@@ -608,7 +611,7 @@ gemv_kernel(const GemvArgs a) {
   // 4096-wide bf16 activations staged whole by one block: 512 chunks of 8 a row, one per thread,
   // so thread tid owns k = 8 tid .. 8 tid + 7 of every row (constant geometry, every row's load in
   // flight at once, conversions in registers)
-  constexpr bool STAGE4K_C = VAR >= 1 && XF == TFD_X_BF16 && !AQ && NT <= 2 && kThreads * 8 == 4096;
+  constexpr bool STAGE4K_C = (VAR == 1 || VAR == 2) && XF == TFD_X_BF16 && !AQ && NT <= 2 && kThreads * 8 == 4096;
   constexpr bool stage4k = STAGE4K_C;
   // (in a cluster split each block scales by the max over its own k range, and its partial sums
   // are scaled back before the cluster sums them: power-of-two scalings are exact, so the logits
@@ -1102,7 +1105,7 @@ gemv_kernel(const GemvArgs a) {
     const int64_t row_lo = row_off + gi * GR + tile * 16 + g;
     float rs0 = 1.0f, rs1 = 1.0f;
     if (WF == TFD_W_FP8_ROW) {
-      if (FASTK && tile == mt) {
+      if (FASTK && CSC == 1 && tile == mt) {  // (a split's leader finishes the previous group)
         rs0 = rs_pref[0];
         rs1 = rs_pref[1];
       } else {
@@ -1144,6 +1147,21 @@ gemv_kernel(const GemvArgs a) {
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
   int rb = 0;
   const int mr = warp & 3, nr = warp >> 2;  // reducer role of warps < 4 * NT
+  // Cluster split: the blocks meet on a split cluster barrier, one group behind. At the end of
+  // group j every block waits for the barrier phase of group j - 1 (long complete unless a block
+  // lags by a whole group), the leader then sums group j - 1's partials from every block's shared
+  // memory, and each block stores its partials of group j and arrives. A block writes a partial
+  // buffer again two groups on, after its wait has seen the leader's arrival behind its read.
+  auto cluster_take = [&](int64_t gp, int pb) {
+    if (crank == 0 && warp < 4 * NT) {
+      float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int q = 0; q < csplit; ++q) {  // blocks in rank order
+        const float4 u = cg::this_cluster().map_shared_rank(cpart, q)[(pb * 4 * NT + warp) * 32 + lane];
+        v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+      }
+      finish_tile(gp, mr, nr * 8 + 2 * t, v, 0);
+    }
+  };
   // The end of group gi: k-slice partials summed, epilogue.
   auto group_end = [&](int64_t gi, int j) {
     if constexpr (FFMA) {
@@ -1191,6 +1209,10 @@ gemv_kernel(const GemvArgs a) {
     }
     __syncthreads();
     if (dyn && claimer) s_q[(j + 3) & 3] = claim();
+    if (csplit > 1 && j > 0) {  // (a split's groups are consecutive: the previous one is gi - 1)
+      asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+      cluster_take(gi - 1, rb ^ 1);
+    }
     if (warp < 4 * NT) {
       // warp index = ks * 4 + mt, so the partials of row tile mr are warps mr, 4+mr, 8+mr, 12+mr.
       float4 v = red[((rb * kWarps + mr) * NT + nr) * 32 + lane];
@@ -1210,16 +1232,7 @@ gemv_kernel(const GemvArgs a) {
       }
     }
     if (csplit > 1) {
-      cg::this_cluster().sync();  // every block's partial of group gi is in its shared memory
-      if (crank == 0 && warp < 4 * NT) {
-        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        for (int q = 0; q < csplit; ++q) {  // blocks in rank order
-          const float4 u = cg::this_cluster().map_shared_rank(cpart, q)[(rb * 4 * NT + warp) * 32 + lane];
-          v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
-        }
-        finish_tile(gi, mr, nr * 8 + 2 * t, v, 0);
-      }
-      // buffer rb is written again two groups on, after the next barrier: the leader has read it
+      asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     }
     }
     rb ^= 1;
@@ -1235,7 +1248,7 @@ gemv_kernel(const GemvArgs a) {
       const unsigned char* qn = fast_ptr(nxt ? gn : gi);
       const uint8_t* sq = BLK ? fast_sp(gi) : nullptr;
       const uint8_t* sqn = BLK ? fast_sp(nxt ? gn : gi) : nullptr;
-      if (WF == TFD_W_FP8_ROW) {
+      if (WF == TFD_W_FP8_ROW && CSC == 1) {
         rs_pref[0] = __ldg(row_scales + gi * GR + mt * 16 + g);
         rs_pref[1] = __ldg(row_scales + gi * GR + mt * 16 + g + 8);
       }
@@ -1266,6 +1279,10 @@ gemv_kernel(const GemvArgs a) {
     }
   }
   if (csplit > 1) {
+    if (g_begin < g_end) {  // the last group's partials
+      asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+      cluster_take(g_end - 1, rb ^ 1);
+    }
     cg::this_cluster().sync();  // the leader has read every block's last partial
     if (crank != 0) return;
   }
@@ -1494,7 +1511,22 @@ tfd_status gemv_launch_k(GemvArgs a, int parts_req, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TFD_ERR_CUDA;
+  auto kc = kern;
+#if TFD_GEMV_FAST
+  // a 4096-wide matrix of whole 64-row groups split over two blocks: the unrolled, check-free
+  // weight loop (one n-tile of row-scaled FP8 weights; four n-tiles measured slower with it)
+  if constexpr (XF == TFD_X_BF16 && KSL == 4 &&
+                ((NT == 1 && WF == TFD_W_FP8_ROW)) &&
+                4096 / (KSL * 4 * E * 2) >= gemv_depth<WF, NT, XF>()) {
+    if (csplit == 2 && a.k == 4096 && a.n % (16 * (16 / KSL)) == 0) {
+      kc = gemv_kernel<WF, XF, NT, gemv_depth<WF, NT, XF>(), KSL, 3>;
+      if (cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit) !=
+          cudaSuccess)
+        return TFD_ERR_CUDA;
+    }
+  }
+#endif
+  if (cudaLaunchKernelEx(&cfg, kc, a) != cudaSuccess) return TFD_ERR_CUDA;
   return tfd_host::launch_status();
 }
 

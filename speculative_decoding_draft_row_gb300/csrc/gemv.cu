@@ -113,7 +113,6 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
                                     int64_t ldt, float* top1_conf, void* ws, size_t ws_bytes,
                                     int32_t* dev_status, void* stream) {
   using tfd_host::aligned;
-  (void)dev_status;  // no device-data errors are possible in this call
   if (!w || !x) return TFD_ERR_INVALID;
   if (wfmt < TFD_W_BF16 || wfmt > TFD_W_FP8_BLOCK32_IL) return TFD_ERR_INVALID;
   if (xfmt < TFD_X_BF16 || xfmt > TFD_X_BF16_E4M3) return TFD_ERR_INVALID;
@@ -163,6 +162,7 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   int parts_used = 0;
   a.parts_used = &parts_used;
   a.trace = g_trace;
+  a.status = dev_status;
   // groups taken from a queue in the workspace (bit-identical results; not with the confidence,
   // whose merge order would then follow the blocks' shares)
   a.queue = (TFD_GEMV_QUEUE && wl.counter != nullptr && need > 0 && top1_conf == nullptr)

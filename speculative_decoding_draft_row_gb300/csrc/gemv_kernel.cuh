@@ -161,6 +161,7 @@ struct GemvArgs {
   int* parts_used;  // host only (never read by the kernel): the launcher stores the part count
   uint64_t* trace;  // TFD_TRACE builds: [blocks][kTraceSlots] phase stamps, or null
   uint32_t* queue;  // group queue counter (zero between calls), or null for a static split
+  int32_t* status;  // device status (TFD_ERR_TIMEOUT from a bounded wait), or null
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -239,6 +240,50 @@ __device__ __forceinline__ float e8m0_scale(uint32_t byte) {
   return byte == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(byte << 23);
 }
 
+// ---- shared-memory barriers of the two-block partial exchange ----
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+// The address of this block's shared-memory word `p` in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+// Waits for the phase of parity `par` of a local mbarrier to complete (acquire, cluster scope).
+// Gives up after about a second of global time: false, and the caller reports TFD_ERR_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t par) {
+  const uint32_t ba = smem_addr(bar);
+  uint32_t ok;
+  uint64_t t0 = 0;
+  for (int it = 0;; ++it) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(ba), "r"(par)
+        : "memory");
+    if (ok) return true;
+    uint64_t now;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+    if (it == 0) t0 = now;
+    else if (now - t0 > 1000000000ull) return false;
+  }
+}
+// One float4 into block 0's shared memory (cluster address `dst`), counted as 16 bytes of the
+// transaction of the mbarrier at cluster address `bar` there. The write needs no fence of its
+// own: the barrier's phase completes only once the bytes have landed.
+__device__ __forceinline__ void st_async_f4(uint32_t dst, float4 v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+
 template <int WF>
 struct WLoad {
   uint32_t r[2][WTraits<WF>::WORDS];  // rows g and g + 8
@@ -286,9 +331,10 @@ struct Layout {
     return (size_t)MT * kMaxRowsPad * 8 + kMaxRowsPad * kWarps * 8 + 2 * kMaxRowsPad * 4 +
            MT * kMaxRowsPad * 8 + kMaxRowsPad * kWarps * 8 + kMaxRowsPad * 4;
   }
-  // group partials of a block for its cluster leader, double-buffered (4 k-slices only)
+  // group partials of a block for its cluster leader, double-buffered, and (up to two n-tiles)
+  // the leader's own partials of its last group (4 k-slices only)
   __host__ __device__ static size_t cpart_bytes() {
-    return KSL == 1 ? 0 : (size_t)2 * 4 * NT * 32 * 16;
+    return KSL == 1 ? 0 : (size_t)(NT == 4 ? 2 : 3) * 4 * NT * 32 * 16;
   }
   __host__ __device__ static size_t smem_bytes(int ssl) {
     return x_bytes(ssl) + red_bytes() + cpart_bytes() + best_bytes();
@@ -327,6 +373,7 @@ gemv_kernel(const GemvArgs a) {
   float2* sjms = sms + MT * kMaxRowsPad;                             // [kWarps][kMaxRowsPad]
   uint32_t* spmax = reinterpret_cast<uint32_t*>(sjms + kWarps * kMaxRowsPad);  // [kMaxRowsPad]
   __shared__ int is_last;
+  __shared__ __align__(8) uint64_t s_full[2], s_empty[2];  // cluster split of two: the exchange
   // FP8 weights run f16 MMAs: each activation row is scaled by a power of two 2^-e_r into f16 range
   // (max |x| in [2^14, 2^15)), which keeps every bf16 activation exact down to 2^-32 of the row's
   // max; the epilogue multiplies by 2^e_r.
@@ -599,6 +646,18 @@ gemv_kernel(const GemvArgs a) {
   }
 
   for (int i = tid; i < MT * kMaxRowsPad; i += kThreads) sbest[i] = 0ull;
+  if (csplit == 2) {
+    // the exchange's barriers, initialised before either block of the pair can reach them (the
+    // pair meets on the cluster barrier before its first group)
+    if (tid == 0) {
+      mbar_init(&s_full[0], 1);
+      mbar_init(&s_full[1], 1);
+      mbar_init(&s_empty[0], 4 * NT);
+      mbar_init(&s_empty[1], 4 * NT);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  }
   if (tid < kMaxRowsPad) { sxmax[tid] = 0u; spmax[tid] = 0u; }
   if (dyn && claimer) {
     s_q[1] = claim();
@@ -1147,11 +1206,38 @@ gemv_kernel(const GemvArgs a) {
     for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
   int rb = 0;
   const int mr = warp & 3, nr = warp >> 2;  // reducer role of warps < 4 * NT
-  // Cluster split: the blocks meet on a split cluster barrier, one group behind. At the end of
-  // group j every block waits for the barrier phase of group j - 1 (long complete unless a block
-  // lags by a whole group), the leader then sums group j - 1's partials from every block's shared
-  // memory, and each block stores its partials of group j and arrives. A block writes a partial
-  // buffer again two groups on, after its wait has seen the leader's arrival behind its read.
+  // Cluster split of more than two: the blocks meet on a split cluster barrier, one group behind.
+  // At the end of group j every block waits for the barrier phase of group j - 1 (long complete
+  // unless a block lags by a whole group), the leader then sums group j - 1's partials from every
+  // block's shared memory, and each block stores its partials of group j and arrives. A block
+  // writes a partial buffer again two groups on, after its wait has seen the leader's arrival
+  // behind its read. (The leader's arrival is relaxed: it has consumed the values it read. A
+  // release would first wait for every load the block has in flight, the weight ring included.)
+  // Cluster split of two: no cluster barrier per group. The second block writes its partials of
+  // group j straight into the leader's buffer j & 1 with asynchronous stores counted by the
+  // leader's mbarrier s_full[j & 1]; the leader keeps its own partials in registers, waits on
+  // s_full one group later, sums, and each of its reducer warps then arrives on the second block's
+  // s_empty[j & 1], which the second block waits for before it writes that buffer again.
+  // the leader's own partial of its last group (split of two): in registers at four n-tiles
+  // (shared memory is full there), else after the two exchange buffers (fewer registers live)
+  float4 vown = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  float4* cown = cpart + 2 * 4 * NT * 32;
+  auto take2 = [&](int64_t gp, int jp) {  // the leader's sum of the pair's group jp (group gp)
+    if (warp < 4 * NT) {
+      const int pb = jp & 1;
+      if (!mbar_wait(&s_full[pb], (uint32_t)(jp >> 1) & 1u)) set_dev_status(a.status, TFD_ERR_TIMEOUT);
+      const float4 u = cpart[(pb * 4 * NT + warp) * 32 + lane];
+      // rank order: the leader's partial, then the second block's
+      float4 v = NT == 4 ? vown : cown[warp * 32 + lane];
+      v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+      __syncwarp();  // every lane of the warp has consumed its slot
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                         cluster_addr(&s_empty[pb], 1))
+                     : "memory");
+      finish_tile(gp, mr, nr * 8 + 2 * t, v, 0);
+    }
+  };
   auto cluster_take = [&](int64_t gp, int pb) {
     if (crank == 0 && warp < 4 * NT) {
       float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -1209,10 +1295,17 @@ gemv_kernel(const GemvArgs a) {
     }
     __syncthreads();
     if (dyn && claimer) s_q[(j + 3) & 3] = claim();
-    if (csplit > 1 && j > 0) {  // (a split's groups are consecutive: the previous one is gi - 1)
+    // (a split's groups are consecutive: the previous one is gi - 1)
+    if (csplit > 2 && j > 0) {
       asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
       cluster_take(gi - 1, rb ^ 1);
     }
+    if (csplit == 2 && j > 0 && crank == 0) take2(gi - 1, j - 1);
+    if (csplit == 2 && crank == 0 && tid == 0)  // group j's bytes from the second block
+      asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                       smem_addr(&s_full[j & 1])),
+                   "r"(4 * NT * 32 * 16)
+                   : "memory");
     if (warp < 4 * NT) {
       // warp index = ks * 4 + mt, so the partials of row tile mr are warps mr, 4+mr, 8+mr, 12+mr.
       float4 v = red[((rb * kWarps + mr) * NT + nr) * 32 + lane];
@@ -1228,16 +1321,32 @@ gemv_kernel(const GemvArgs a) {
           v.x *= sxscale[act0]; v.z *= sxscale[act0];
           v.y *= sxscale[act0 + 1]; v.w *= sxscale[act0 + 1];
         }
-        cpart[(rb * 4 * NT + warp) * 32 + lane] = v;
+        if (csplit == 2) {
+          if (crank == 0) {
+            if (NT == 4) vown = v;
+            else cown[warp * 32 + lane] = v;  // read by this thread at the next group's end
+          } else {
+            const int b = j & 1;  // written again two groups on, once the leader has read it
+            if (j >= 2 && !mbar_wait(&s_empty[b], (uint32_t)((j >> 1) - 1) & 1u))
+              set_dev_status(a.status, TFD_ERR_TIMEOUT);
+            st_async_f4(cluster_addr(cpart + (b * 4 * NT + warp) * 32 + lane, 0), v,
+                        cluster_addr(&s_full[b], 0));
+          }
+        } else {
+          cpart[(rb * 4 * NT + warp) * 32 + lane] = v;
+        }
       }
     }
-    if (csplit > 1) {
-      asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    if (csplit > 2) {
+      if (crank == 0) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+      else asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     }
     }
     rb ^= 1;
     TFD_STAMP(a.trace, 2 + (j < 55 ? j : 55));
   };
+  // (split of two: both blocks' exchange barriers are initialised)
+  if (csplit == 2) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   if constexpr (FASTK) {
     for (int j = 0;; ++j) {
       const int64_t gi = seq_group(j);
@@ -1280,8 +1389,12 @@ gemv_kernel(const GemvArgs a) {
   }
   if (csplit > 1) {
     if (g_begin < g_end) {  // the last group's partials
-      asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-      cluster_take(g_end - 1, rb ^ 1);
+      if (csplit == 2) {
+        if (crank == 0) take2(g_end - 1, (int)(g_end - 1 - g_begin));
+      } else {
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+        cluster_take(g_end - 1, rb ^ 1);
+      }
     }
     cg::this_cluster().sync();  // the leader has read every block's last partial
     if (crank != 0) return;

@@ -149,7 +149,10 @@ tfd_status tfd_quant_fp8(const void* w_bf16, int64_t n, int64_t k, int mode, uin
  *   id_map   device int32 [n] or NULL: the id reported (and compared on ties) for output i is
  *            id_map[i] instead of i (a candidate list or a subset vocabulary, [SUBSET]).
  *   ws       device workspace of tfd_head_gemv_workspace(rows, n, topk, parts) bytes (may be 0).
- *   dev_status device int32 or NULL.
+ *   dev_status device int32 or NULL. A matrix split over a cluster of two blocks (few 64-row
+ *            groups, or 17-32 rows of a 4096-wide matrix) exchanges partial sums through bounded
+ *            waits; one that gives up (after about a second) stores TFD_ERR_TIMEOUT there and the
+ *            call's outputs are then undefined. No other device-data errors exist in this call.
  * Refused: rows outside 1..32 (1..16 for fp32 activations); topk > 512 or > n; x aliasing y; NULL or misaligned pointers;
  *   rows * k too large for the activation tile (TFD_ERR_UNSUPPORTED, see tfd_head_gemv_max_k).
  */

@@ -206,6 +206,17 @@ __device__ __forceinline__ void mma_e4m3_16832_z(float (&d)[4], uint32_t a0, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
+// The same MMA accumulating into d (row-scaled codes: no per-block scale between the MMAs).
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Two floats -> two E4M3 codes (byte 0 = lo, byte 1 = hi), RNE, saturating to +-448.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   uint16_t r;
@@ -344,12 +355,13 @@ struct Layout {
 // VAR: 0 the general form; 1 a 4096-wide matrix staged by one block (no cluster split) with bf16
 // activations: constant staging geometry; 2 that, plus the unrolled check-free weight loop (n a
 // multiple of the group rows); 3 the unrolled check-free weight loop of a 4096-wide matrix split
-// over a cluster of two (a small matrix, e.g. the attention output projection). The host picks
-// the instantiation.
+// over a cluster of two (a small matrix, e.g. the attention output projection); 4 the general form
+// without a cluster split (none of the split's code, so fewer registers live). The host picks the
+// instantiation.
 template <int WF, int XF, int NT, int D, int KSL, int VAR = 0>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? TFD_GEMV_MINB_NT1 : 1)
 gemv_kernel(const GemvArgs a) {
-  constexpr bool FASTP = VAR >= 2;
+  constexpr bool FASTP = VAR == 2 || VAR == 3;
   constexpr int CSC = VAR == 3 ? 2 : 1;  // the cluster split the fast loop is built for
   using L = Layout<WF, XF, NT, KSL>;
   constexpr int MT = L::MT;
@@ -401,7 +413,7 @@ gemv_kernel(const GemvArgs a) {
   // cluster cid takes k-slices 4 crank .. 4 crank + 3 of every group of the cluster; the leader
   // (crank 0) sums the blocks' partials in rank order and runs the epilogue.
   namespace cg = cooperative_groups;
-  const int csplit = (KSL == 1 || VAR == 1 || VAR == 2) ? 1 : VAR == 3 ? 2 : a.csplit;
+  const int csplit = (KSL == 1 || VAR == 1 || VAR == 2 || VAR == 4) ? 1 : VAR == 3 ? 2 : a.csplit;
   const int crank = csplit > 1 ? (int)cg::this_cluster().block_rank() : 0;
   const int cid = blockIdx.x / csplit;
   const int kstep0 = crank * KSL * ssl;  // first step of this block's k range
@@ -1023,7 +1035,8 @@ gemv_kernel(const GemvArgs a) {
       (void)acc;
     } else if constexpr (AQ) {
       // MMA j (k = 32) takes codes [8j, 8j + 8) of each thread's 16: one scale block in the block-32
-      // forms. Each MMA starts from zero and is added in fp32 (times its block's scale).
+      // forms, where each MMA starts from zero and is added in fp32 times its block's scale; the
+      // row-scaled form accumulates in the MMAs.
       uint4 xq[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) xq[nt] = xs[(sg * NT + nt) * 32 + lane];
@@ -1032,11 +1045,17 @@ gemv_kernel(const GemvArgs a) {
         const float sc = BLK ? e8m0_scale((b.scb >> (8 * j)) & 0xFFu) : 1.0f;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          float c[4];
-          mma_e4m3_16832_z(c, b.r[0][2 * j], b.r[1][2 * j], b.r[0][2 * j + 1], b.r[1][2 * j + 1],
-                           j == 0 ? xq[nt].x : xq[nt].z, j == 0 ? xq[nt].y : xq[nt].w);
+          if (BLK) {
+            float c[4];
+            mma_e4m3_16832_z(c, b.r[0][2 * j], b.r[1][2 * j], b.r[0][2 * j + 1], b.r[1][2 * j + 1],
+                             j == 0 ? xq[nt].x : xq[nt].z, j == 0 ? xq[nt].y : xq[nt].w);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc[nt][i] = BLK ? fmaf(sc, c[i], acc[nt][i]) : acc[nt][i] + c[i];
+            for (int i = 0; i < 4; ++i) acc[nt][i] = fmaf(sc, c[i], acc[nt][i]);
+          } else {  // one scale per row: the MMAs accumulate in place
+            mma_e4m3_16832(acc[nt], b.r[0][2 * j], b.r[1][2 * j], b.r[0][2 * j + 1],
+                           b.r[1][2 * j + 1], j == 0 ? xq[nt].x : xq[nt].z,
+                           j == 0 ? xq[nt].y : xq[nt].w);
+          }
         }
       }
     } else if constexpr (BLK) {
@@ -1606,7 +1625,19 @@ tfd_status gemv_launch_k(GemvArgs a, int parts_req, cudaStream_t stream) {
       }
     }
 #endif
-    kern<<<parts, kThreads, smem, stream>>>(a);
+    auto k1 = kern;
+    // the FP8 block-32 forms at two n-tiles and the W8A8 forms: the general loop without the
+    // split's code (measured slower with it)
+    if constexpr (KSL == 4 && NT <= 2 &&
+                  ((XF == TFD_X_BF16 && NT == 2 &&
+                    (WF == TFD_W_FP8_BLOCK32 || WF == TFD_W_FP8_BLOCK32_IL)) ||
+                   XF == TFD_X_BF16_E4M3)) {
+      k1 = gemv_kernel<WF, XF, NT, gemv_depth<WF, NT, XF>(), KSL, 4>;
+      if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit) !=
+          cudaSuccess)
+        return TFD_ERR_CUDA;
+    }
+    k1<<<parts, kThreads, smem, stream>>>(a);
     return tfd_host::launch_status();
   }
   constexpr int E = WTraits<WF>::E;

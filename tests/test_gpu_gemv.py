@@ -141,6 +141,47 @@ def test_block32_interleaved_equals_plain_bit_for_bit(n, k, rows, xf32):
     assert_fp32_close(np32(y1), acc, S, "interleaved block-32 logits")
 
 
+def scaled_block_case(n, k, rows, tid):
+    """FP8 block-32 codes of weights whose 32 x 32 blocks differ in magnitude (factors from 2^-6
+    to 2^5, some blocks all zero), so that neighbouring blocks of a row block get different E8M0
+    scales (and zero scale bytes)."""
+    rng = np.random.default_rng(tid)
+    w = inputs.normal_bf16((n, k), 0.05, tid).float().numpy()
+    f = rng.choice(np.array([0.0, 2.0 ** -6, 0.3, 1.0, 1.0, 1.0, 5.5, 32.0], np.float32),
+                   size=(n // 32, k // 32))
+    w = w * np.repeat(np.repeat(f, 32, 0), 32, 1)
+    w = torch.from_numpy(w).to(torch.bfloat16).float().numpy()
+    c, sc = quant_fp8_block32(w)
+    x = inputs.normal_bf16((rows, k), 1.0, tid + 1)
+    return c, sc, x
+
+
+@pytest.mark.parametrize("n,k,rows", [(2048, 4096, 16), (2080, 1088, 5), (4096, 4096, 1),
+                                      (2048, 4096, 32)])
+def test_block32_scales_that_differ_between_blocks(n, k, rows):
+    """Block scales that change from one 32-wide block to the next (and all-zero blocks): the
+    plain and interleaved layouts, W16 and W8A8, against the oracle; the two layouts bit-equal."""
+    need_gpu()
+    c, sc, x = scaled_block_case(n, k, rows, 380 + rows)
+    xn = x.float().numpy()
+    cd, sd, xd = torch.from_numpy(c).cuda(), torch.from_numpy(sc).cuda(), x.cuda()
+    il = tfd.tfd_fp8_block32_relayout(cd, True)
+    y0, v0, i0 = tfd.tfd_head_gemv(cd, tfd.W_FP8_BLOCK32, sd, xd, tfd.OUT_F32, topk=16)
+    y1, v1, i1 = tfd.tfd_head_gemv(il, tfd.W_FP8_BLOCK32_IL, sd, xd, tfd.OUT_F32, topk=16)
+    torch.cuda.synchronize()
+    assert same_bits(np32(y0), np32(y1)) and torch.equal(i0, i1) and same_bits(np32(v0), np32(v1))
+    acc = og.gemv_acc(c, xn, og.W_FP8_BLOCK32, sc)
+    S = og.gemv_abs_scale(c, xn, og.W_FP8_BLOCK32, sc)
+    assert_fp32_close(np32(y1), acc, S, "block-32 logits, mixed scales")
+    assert_topk_valid(np32(v1), i1.cpu().numpy(), acc, S, 16, what="top-16, mixed scales")
+    if rows <= 16:
+        y2, _, _ = tfd.tfd_head_gemv(il, tfd.W_FP8_BLOCK32_IL, sd, xd, tfd.OUT_F32, act_e4m3=True)
+        torch.cuda.synchronize()
+        acc = og.gemv_acc(c, xn, og.W_FP8_BLOCK32, sc, act_fp8=True)
+        S = og.gemv_abs_scale(c, xn, og.W_FP8_BLOCK32, sc, act_fp8=True)
+        assert_fp32_close(np32(y2), acc, S, "W8A8 block-32 logits, mixed scales")
+
+
 W8A8_SHAPES = [(4096, 4096, 1, tfd.W_FP8_ROW), (4096, 4096, 10, tfd.W_FP8_ROW),
                (4096, 4096, 32, tfd.W_FP8_ROW), (2080, 4096, 25, tfd.W_FP8_BLOCK32_IL),
                (1000, 272, 3, tfd.W_FP8_ROW), (4096, 11008, 4, tfd.W_FP8_ROW),

@@ -106,6 +106,10 @@ extern "C" int64_t tfd_head_gemv_max_k(int rows, int xfmt) {
   return best;
 }
 
+// gemv_tc.cu: the tcgen05 form for 17-32 rows of bf16 (sets *taken when it takes the call).
+tfd_status gemv_tc_launch(const tfd_gemv::GemvArgs& g, int wfmt, int xfmt, int parts_req,
+                          cudaStream_t stream, bool* taken);
+
 extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scales, int64_t n,
                                     int64_t k, const void* x, int xfmt, int rows, int64_t ldx,
                                     int out_mode, void* y, int64_t ldy, int topk, int parts,
@@ -178,6 +182,10 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   a.ngroups = 0;  // set by the launcher for its group size
   cudaStream_t s = tfd_host::as_stream(stream);
   tfd_status st;
+  bool taken = false;
+  st = gemv_tc_launch(a, wfmt, xfmt, parts, s, &taken);  // 17-32 rows of bf16 on tcgen05
+  if (taken) return st;
+  if (st != TFD_OK) return st;
   if (wfmt == TFD_W_FP8_ROW) st = gemv_launch_x<TFD_W_FP8_ROW>(a, xfmt, parts, s);
   else if (wfmt == TFD_W_FP8_BLOCK32) st = gemv_launch_x<TFD_W_FP8_BLOCK32>(a, xfmt, parts, s);
   else if (wfmt == TFD_W_FP8_BLOCK32_IL)

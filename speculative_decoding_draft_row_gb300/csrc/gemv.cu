@@ -184,8 +184,13 @@ extern "C" tfd_status tfd_head_gemv(const void* w, int wfmt, const void* w_scale
   tfd_status st;
   bool taken = false;
   st = gemv_tc_launch(a, wfmt, xfmt, parts, s, &taken);  // 17-32 rows of bf16 on tcgen05
-  if (taken) return st;
   if (st != TFD_OK) return st;
+  if (taken) {
+    if (topk <= 1) return st;
+    return tfd_internal::topk_launch(a.logits, rows, n, a.ld_logits, topk, id_map, top_vals,
+                                     top_ids, ldt, wl.submax, wl.part_max, parts_used, wl.topk_ws,
+                                     wl.topk_bytes, s);
+  }
   if (wfmt == TFD_W_FP8_ROW) st = gemv_launch_x<TFD_W_FP8_ROW>(a, xfmt, parts, s);
   else if (wfmt == TFD_W_FP8_BLOCK32) st = gemv_launch_x<TFD_W_FP8_BLOCK32>(a, xfmt, parts, s);
   else if (wfmt == TFD_W_FP8_BLOCK32_IL)

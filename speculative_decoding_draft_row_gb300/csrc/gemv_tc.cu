@@ -16,8 +16,9 @@
 // of two tensor-memory column buffers, each stage released by a tcgen05 commit); warps 2-5 read a
 // finished accumulator (one row of 32 outputs a thread), and the second block of the pair sends
 // its half into the leader's shared memory with asynchronous stores, where the leader adds it in
-// rank order and runs the epilogue (fp32 logits, the running top-1 of each activation row). At the
-// end each leader writes its part's keys and the last one to finish joins the parts.
+// rank order and runs the epilogue (fp32 logits, the running top-1 of each activation row, or for
+// a fused top-k > 1 each 16-row sub-group's maximum and the part's maximum per row). At the end
+// each leader writes its part's keys and the last one to finish joins the parts.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -50,7 +51,8 @@ constexpr int kOffBar = kOffInbox + kInboxBytes;  // mbarriers (8 bytes each)
 constexpr int kNumBars = 2 * kStages + 1 + 2 + 2 + 2;
 constexpr int kOffBest = kOffBar + kNumBars * 8 + 8;  // (+ the tensor-memory address)
 constexpr int kOffJoin = kOffBest + 4 * kN * 8;
-constexpr int kSmemUsed = kOffJoin + kN * 8 + 16;
+constexpr int kOffPmax = kOffJoin + kN * 8;
+constexpr int kSmemUsed = kOffPmax + kN * 4 + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base
 
 struct TcArgs {
@@ -58,10 +60,12 @@ struct TcArgs {
   int rows;
   int parts;  // clusters
   int64_t ngroups;
-  float* y;  // fp32 logits [rows][ldy], or null
+  float* y;  // fp32 logits [rows][ldy] (the top-k's logits when topk > 1), or null
   int64_t ldy;
-  int topk;  // 0 or 1
+  int topk;
   const int32_t* id_map;
+  uint32_t* submax;    // topk > 1: [rows][ceil(n / 16)]
+  uint32_t* part_max;  // topk > 1: [parts][rows]
   uint64_t* part_keys;  // [parts][rows]
   uint32_t* counter;
   float* top_vals;
@@ -208,7 +212,9 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ C
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + kNumBars * 8);
   uint64_t* sbest = reinterpret_cast<uint64_t*>(smem + kOffBest);
   uint64_t* sjoin = reinterpret_cast<uint64_t*>(smem + kOffJoin);
+  uint32_t* spmax = reinterpret_cast<uint32_t*>(smem + kOffPmax);
 
+  if (tid < kN) spmax[tid] = 0u;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       bar_init(full(s), 1);
@@ -257,7 +263,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ C
     }
   } else if (warp == 1) {
     if (lane == 0 && ng > 0) {
-      if (!bar_wait(xfull, 0)) timed_out = true;
+      if (!bar_wait(xfull, 0)) timed_out = true;  // (the first wait of this thread)
       fence_after();
       int it = 0;
       for (int j = 0; j < ng; ++j) {
@@ -269,11 +275,11 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ C
           const int s = it % kStages;
           if (!timed_out && !bar_wait(full(s), (uint32_t)(it / kStages) & 1u)) timed_out = true;
           fence_after();
-          const uint32_t as = s_stage + (uint32_t)(s * kStageBytes);
-          const uint32_t bs = s_x + (uint32_t)(kb * kXBlockBytes);
+          const uint64_t da = sdesc(s_stage + (uint32_t)(s * kStageBytes));
+          const uint64_t db = sdesc(s_x + (uint32_t)(kb * kXBlockBytes));
 #pragma unroll
-          for (int kk = 0; kk < kKB / 16; ++kk)  // 16 k (32 bytes) per MMA
-            mma(d, sdesc(as + 32u * kk), sdesc(bs + 32u * kk), (kb | kk) != 0);
+          for (int kk = 0; kk < kKB / 16; ++kk)  // 16 k (32 bytes, 2 address units) per MMA
+            mma(d, da + 2u * kk, db + 2u * kk, (kb | kk) != 0);
           mma_commit(empty(s));  // the stage is free once these MMAs have read it
         }
         mma_commit(tfull(buf));  // the group's accumulator is complete
@@ -319,13 +325,23 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ C
       __syncwarp();  // every lane has consumed its row
       if (lane == 0) bar_arrive_remote(to_cluster(iempty, 1));
       const int64_t row = g * kM + rl;
-      if (row < a.n) {
-        const int32_t id = a.id_map ? __ldg(a.id_map + row) : (int32_t)row;
+      const bool in = row < a.n;
+      const int32_t id = in ? (a.id_map ? __ldg(a.id_map + row) : (int32_t)row) : 0;
+      const int64_t S = (a.n + 15) / 16;
 #pragma unroll
-        for (int c = 0; c < kN; ++c) {
-          if (c < a.rows) {
-            if (a.y) a.y[(int64_t)c * a.ldy + row] = v[c];
-            if (a.topk == 1) best[c] = umax64(best[c], make_key(v[c], id));
+      for (int c = 0; c < kN; ++c) {
+        if (c < a.rows) {  // warp-uniform
+          if (in && a.y) a.y[(int64_t)c * a.ldy + row] = v[c];
+          if (a.topk == 1 && in) best[c] = umax64(best[c], make_key(v[c], id));
+          if (a.topk > 1) {  // the 16 rows of a sub-group are 16 lanes of this warp
+            uint32_t m = in ? value_key(v[c]) : 0u;
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const int64_t sg = row / 16;
+            if ((lane & 15) == 0 && sg < S) {
+              a.submax[(int64_t)c * S + sg] = m;
+              atomicMax(&spmax[c], m);
+            }
           }
         }
       }
@@ -351,7 +367,12 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ C
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
   }
-  if (crank != 0 || a.topk != 1) return;
+  if (crank != 0) return;
+  if (a.topk > 1) {
+    if (tid < a.rows) a.part_max[(int64_t)cid * a.rows + tid] = spmax[tid];
+    return;
+  }
+  if (a.topk != 1) return;
   __shared__ int is_last;
   if (tid < a.rows) {
     uint64_t m = sbest[tid];
@@ -411,7 +432,7 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, ui
 }  // namespace tfd_gemv_tc
 
 // Takes the call when it is this kernel's (bf16 weights and rows, 17-32 rows, a k range of at
-// most 2048 per block of the pair in whole 64-wide blocks, fp32 logits or none, top-1 or none, no
+// most 2048 per block of the pair in whole 64-wide blocks, fp32 logits or none, any top-k, no
 // confidence); *taken = false leaves it to the register-ring kernel.
 tfd_status gemv_tc_launch(const tfd_gemv::GemvArgs& g, int wfmt, int xfmt, int parts_req,
                           cudaStream_t stream, bool* taken) {
@@ -422,7 +443,9 @@ tfd_status gemv_tc_launch(const tfd_gemv::GemvArgs& g, int wfmt, int xfmt, int p
 #endif
   if (wfmt != TFD_W_BF16 || xfmt != TFD_X_BF16 || g.rows < 17 || g.rows > 32) return TFD_OK;
   if (g.k % (2 * kKB) != 0 || g.k / 2 > kMaxKHalf) return TFD_OK;
-  if (g.topk > 1 || g.top1_conf != nullptr) return TFD_OK;
+  if (g.top1_conf != nullptr) return TFD_OK;
+  if (g.topk > 1 && (g.submax == nullptr || g.part_max == nullptr || g.logits == nullptr))
+    return TFD_OK;
   if (g.out_mode != TFD_OUT_NONE && g.out_mode != TFD_OUT_F32) return TFD_OK;
   if ((g.ldx * 2) % 16 != 0 || (reinterpret_cast<uintptr_t>(g.x) & 15) != 0) return TFD_OK;
   CUtensorMap tw, tx;
@@ -447,10 +470,13 @@ tfd_status gemv_tc_launch(const tfd_gemv::GemvArgs& g, int wfmt, int xfmt, int p
   if (p > a.ngroups) p = a.ngroups;
   if (p > tfd_gemv::kMaxParts) p = tfd_gemv::kMaxParts;
   a.parts = (int)p;
-  a.y = g.out_mode == TFD_OUT_F32 ? reinterpret_cast<float*>(g.y) : nullptr;
-  a.ldy = g.ldy;
+  // a top-k > 1 ranks the fp32 logits (in y, or in the workspace when there is no output)
+  a.y = g.topk > 1 ? g.logits : g.out_mode == TFD_OUT_F32 ? reinterpret_cast<float*>(g.y) : nullptr;
+  a.ldy = g.topk > 1 ? g.ld_logits : g.ldy;
   a.topk = g.topk;
   a.id_map = g.id_map;
+  a.submax = g.submax;
+  a.part_max = g.part_max;
   a.part_keys = g.part_keys;
   a.counter = g.counter;
   a.top_vals = g.top_vals;

@@ -16,9 +16,10 @@
 // of two tensor-memory column buffers, each stage released by a tcgen05 commit); warps 2-5 read a
 // finished accumulator (one row of 32 outputs a thread), and the second block of the pair sends
 // its half into the leader's shared memory with asynchronous stores, where the leader adds it in
-// rank order and runs the epilogue (fp32 logits, the running top-1 of each activation row, or for
-// a fused top-k > 1 each 16-row sub-group's maximum and the part's maximum per row). At the end
-// each leader writes its part's keys and the last one to finish joins the parts.
+// rank order and runs the epilogue (fp32 logits, the running top-1 of each activation row and the
+// online softmax state of its confidence, or for a fused top-k > 1 each 16-row sub-group's maximum
+// and the part's maximum per row). At the end each leader writes its part's keys (and softmax
+// states) and the last one to finish joins the parts.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -66,6 +67,8 @@ struct TcArgs {
   const int32_t* id_map;
   uint32_t* submax;    // topk > 1: [rows][ceil(n / 16)]
   uint32_t* part_max;  // topk > 1: [parts][rows]
+  float* top1_conf;    // topk == 1: [rows] softmax probability of the top-1, or null
+  float2* part_ms;     // with the confidence: [parts][rows] (max, sum of exp(l - max))
   uint64_t* part_keys;  // [parts][rows]
   uint32_t* counter;
   float* top_vals;
@@ -183,6 +186,7 @@ __device__ __forceinline__ void st_async4(uint32_t dst, float a, float b, float 
       : "memory");
 }
 
+template <bool CONF>  // the top-1 confidence (a second instantiation: its state costs registers)
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
                const TcArgs a) {
@@ -290,8 +294,13 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ C
     const int q = warp & 3;
     const int rl = 32 * q + lane;
     uint64_t best[kN];
+    float2 ms[CONF ? kN : 1];  // online softmax state of this thread's outputs (the confidence)
+    constexpr bool want_conf = CONF;
 #pragma unroll
-    for (int c = 0; c < kN; ++c) best[c] = 0ull;
+    for (int c = 0; c < kN; ++c) {
+      best[c] = 0ull;
+      if (CONF) ms[CONF ? c : 0] = make_float2(-INFINITY, 0.0f);
+    }
     for (int j = 0; j < ng; ++j) {
       const int buf = j & 1;
       const int64_t g = g_begin + j;
@@ -333,6 +342,15 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ C
         if (c < a.rows) {  // warp-uniform
           if (in && a.y) a.y[(int64_t)c * a.ldy + row] = v[c];
           if (a.topk == 1 && in) best[c] = umax64(best[c], make_key(v[c], id));
+          if (CONF && in && v[c] > -INFINITY) {  // NaN and -inf add nothing
+            float2& m = ms[CONF ? c : 0];
+            if (v[c] > m.x) {
+              m.y = m.y * expf(m.x - v[c]) + 1.0f;
+              m.x = v[c];
+            } else {
+              m.y += expf(v[c] - m.x);
+            }
+          }
           if (a.topk > 1) {  // the 16 rows of a sub-group are 16 lanes of this warp
             uint32_t m = in ? value_key(v[c]) : 0u;
 #pragma unroll
@@ -348,12 +366,23 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ C
     }
     if (crank == 0 && a.topk == 1) {
       // the part's best of each activation row: lanes, then the four warps in a fixed order
+      float2* sms = reinterpret_cast<float2*>(inbox);  // (the inbox is no longer written)
+      // every epilogue warp has read its rows of the last group from the inbox
+      asm volatile("bar.sync 1, 128;" ::: "memory");
 #pragma unroll
       for (int c = 0; c < kN; ++c) {
         uint64_t kk = best[c];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) kk = umax64(kk, shfl_xor_u64(kk, o));
         if (lane == 0) sbest[q * kN + c] = kk;
+        if (CONF) {
+          float2 m = ms[CONF ? c : 0];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+            m = tfd_gemv::ms_merge(m, make_float2(__shfl_xor_sync(0xffffffffu, m.x, o),
+                                                  __shfl_xor_sync(0xffffffffu, m.y, o)));
+          if (lane == 0) sms[q * kN + c] = m;
+        }
       }
     }
   }
@@ -374,10 +403,18 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ C
   }
   if (a.topk != 1) return;
   __shared__ int is_last;
+  constexpr bool want_conf = CONF;
+  float2* sms = reinterpret_cast<float2*>(inbox);
+  float2* sjms = sms + 4 * kN;  // [warps][rows] of the join
   if (tid < a.rows) {
     uint64_t m = sbest[tid];
     for (int w = 1; w < 4; ++w) m = umax64(m, sbest[w * kN + tid]);
     a.part_keys[(int64_t)cid * a.rows + tid] = m;
+    if (want_conf) {
+      float2 qm = sms[tid];
+      for (int w = 1; w < 4; ++w) qm = tfd_gemv::ms_merge(qm, sms[w * kN + tid]);
+      a.part_ms[(int64_t)cid * a.rows + tid] = qm;
+    }
   }
   if (tid < kN) sjoin[tid] = 0ull;
   __threadfence();
@@ -390,11 +427,29 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ C
   for (int i = tid; i < tot; i += kThreads)
     atomicMax(reinterpret_cast<unsigned long long*>(&sjoin[i % a.rows]),
               (unsigned long long)__ldcg(a.part_keys + i));
+  if (want_conf) {
+    // parts merged in a fixed order: p = tid, tid + 192, ..., then lanes, then warps
+    for (int r = 0; r < a.rows; ++r) {
+      float2 qm = make_float2(-INFINITY, 0.0f);
+      for (int p = tid; p < a.parts; p += kThreads)
+        qm = tfd_gemv::ms_merge(qm, __ldcg(a.part_ms + (int64_t)p * a.rows + r));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+        qm = tfd_gemv::ms_merge(qm, make_float2(__shfl_xor_sync(0xffffffffu, qm.x, o),
+                                                __shfl_xor_sync(0xffffffffu, qm.y, o)));
+      if (lane == 0) sjms[warp * kN + r] = qm;
+    }
+  }
   __syncthreads();
   if (tid < a.rows) {
     const uint64_t key = sjoin[tid];
     a.top_vals[tid * a.ldt] = key_value(key);
     a.top_ids[tid * a.ldt] = key_id(key);
+    if (want_conf) {
+      float2 qm = make_float2(-INFINITY, 0.0f);
+      for (int w = 0; w < kThreads / 32; ++w) qm = tfd_gemv::ms_merge(qm, sjms[w * kN + tid]);
+      a.top1_conf[tid] = qm.y > 0.0f ? 1.0f / qm.y : __uint_as_float(0x7FC00000u);
+    }
   }
   if (tid == 0) *a.counter = 0u;  // leave the workspace zeroed
 }
@@ -432,7 +487,7 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, ui
 }  // namespace tfd_gemv_tc
 
 // Takes the call when it is this kernel's (bf16 weights and rows, 17-32 rows, a k range of at
-// most 2048 per block of the pair in whole 64-wide blocks, fp32 logits or none, any top-k, no
+// most 2048 per block of the pair in whole 64-wide blocks, fp32 logits or none, any top-k, the
 // confidence); *taken = false leaves it to the register-ring kernel.
 tfd_status gemv_tc_launch(const tfd_gemv::GemvArgs& g, int wfmt, int xfmt, int parts_req,
                           cudaStream_t stream, bool* taken) {
@@ -443,7 +498,6 @@ tfd_status gemv_tc_launch(const tfd_gemv::GemvArgs& g, int wfmt, int xfmt, int p
 #endif
   if (wfmt != TFD_W_BF16 || xfmt != TFD_X_BF16 || g.rows < 17 || g.rows > 32) return TFD_OK;
   if (g.k % (2 * kKB) != 0 || g.k / 2 > kMaxKHalf) return TFD_OK;
-  if (g.top1_conf != nullptr) return TFD_OK;
   if (g.topk > 1 && (g.submax == nullptr || g.part_max == nullptr || g.logits == nullptr))
     return TFD_OK;
   if (g.out_mode != TFD_OUT_NONE && g.out_mode != TFD_OUT_F32) return TFD_OK;
@@ -452,14 +506,16 @@ tfd_status gemv_tc_launch(const tfd_gemv::GemvArgs& g, int wfmt, int xfmt, int p
   if (!map_2d(&tw, g.w, (uint64_t)g.k, (uint64_t)g.n, (uint64_t)g.k * 2, kKB, kM) ||
       !map_2d(&tx, g.x, (uint64_t)g.k, (uint64_t)g.rows, (uint64_t)g.ldx * 2, kKB, kN))
     return TFD_OK;
-  static bool attr_set[64] = {};
+  const bool conf = g.topk == 1 && g.top1_conf != nullptr;
+  auto kern = conf ? gemv_tc_kernel<true> : gemv_tc_kernel<false>;
+  static bool attr_set[2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return TFD_ERR_CUDA;
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
+  if (dev < 64 && !attr_set[conf][dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+        cudaSuccess)
       return TFD_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[conf][dev] = true;
   }
   TcArgs a{};
   a.n = g.n;
@@ -477,6 +533,8 @@ tfd_status gemv_tc_launch(const tfd_gemv::GemvArgs& g, int wfmt, int xfmt, int p
   a.id_map = g.id_map;
   a.submax = g.submax;
   a.part_max = g.part_max;
+  a.top1_conf = g.top1_conf;
+  a.part_ms = g.part_ms;
   a.part_keys = g.part_keys;
   a.counter = g.counter;
   a.top_vals = g.top_vals;
@@ -485,6 +543,6 @@ tfd_status gemv_tc_launch(const tfd_gemv::GemvArgs& g, int wfmt, int xfmt, int p
   a.status = g.status;
   if (g.parts_used != nullptr) *g.parts_used = a.parts;
   *taken = true;
-  gemv_tc_kernel<<<2 * a.parts, kThreads, kSmemBytes, stream>>>(tw, tx, a);
+  kern<<<2 * a.parts, kThreads, kSmemBytes, stream>>>(tw, tx, a);
   return tfd_host::launch_status();
 }

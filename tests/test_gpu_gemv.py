@@ -287,7 +287,8 @@ def test_fused_topk_ranks_the_fp32_logits_in_every_output_mode(out_mode, rows, n
     assert torch.equal(ti2, ti) and same_bits(np32(tv2), np32(tv))
 
 
-@pytest.mark.parametrize("wfmt,rows", [(tfd.W_BF16, 1), (tfd.W_BF16, 16), (tfd.W_FP8_ROW, 5)])
+@pytest.mark.parametrize("wfmt,rows", [(tfd.W_BF16, 1), (tfd.W_BF16, 16), (tfd.W_FP8_ROW, 5),
+                                       (tfd.W_BF16, 24)])
 def test_top1_confidence(wfmt, rows):
     need_gpu()
     case = make_case(20480, 4096, rows, wfmt, tid=380, tie_frac=0.01)

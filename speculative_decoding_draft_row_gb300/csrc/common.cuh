@@ -97,6 +97,14 @@ __device__ __forceinline__ uint2 ldg_stream8(const void* p, uint64_t pol) {
   return v;
 }
 
+// ---- a planted failure for the bounded waits (TFD_TEST_STALL_EXCHANGE builds only) --------------
+// A build with -DTFD_TEST_STALL_EXCHANGE=1 has the second block of every two-block cluster split
+// drop its partial sums instead of sending them, so the leader's bounded waits run out and report
+// TFD_ERR_TIMEOUT in the device status (tests of the failure path); the default build sends them.
+#ifndef TFD_TEST_STALL_EXCHANGE
+#define TFD_TEST_STALL_EXCHANGE 0
+#endif
+
 // ---- phase timestamps (TFD_TRACE builds only) -----------------------------------------------------
 // A build with -DTFD_TRACE=1 records the global nanosecond timer at fixed points of a kernel, one
 // row of kTraceSlots stamps per block, into a caller-given device buffer (tfd_trace_set); the

@@ -1348,8 +1348,9 @@ gemv_kernel(const GemvArgs a) {
             const int b = j & 1;  // written again two groups on, once the leader has read it
             if (j >= 2 && !mbar_wait(&s_empty[b], (uint32_t)((j >> 1) - 1) & 1u))
               set_dev_status(a.status, TFD_ERR_TIMEOUT);
-            st_async_f4(cluster_addr(cpart + (b * 4 * NT + warp) * 32 + lane, 0), v,
-                        cluster_addr(&s_full[b], 0));
+            if (!TFD_TEST_STALL_EXCHANGE)
+              st_async_f4(cluster_addr(cpart + (b * 4 * NT + warp) * 32 + lane, 0), v,
+                          cluster_addr(&s_full[b], 0));
           }
         } else {
           cpart[(rb * 4 * NT + warp) * 32 + lane] = v;

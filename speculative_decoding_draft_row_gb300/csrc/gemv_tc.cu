@@ -318,7 +318,8 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ C
         const uint32_t dst = to_cluster(sa(inbox + rl * kN), 0);
         const uint32_t rb = to_cluster(ifull, 0);
 #pragma unroll
-        for (int c = 0; c < kN; c += 4) st_async4(dst + 4u * c, v[c], v[c + 1], v[c + 2], v[c + 3], rb);
+        for (int c = 0; c < kN; c += 4)
+          if (!TFD_TEST_STALL_EXCHANGE) st_async4(dst + 4u * c, v[c], v[c + 1], v[c + 2], v[c + 3], rb);
         continue;
       }
       if (warp == 2 && lane == 0) bar_expect_tx(ifull, kInboxBytes);

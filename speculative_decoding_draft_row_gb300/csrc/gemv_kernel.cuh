@@ -688,6 +688,10 @@ gemv_kernel(const GemvArgs a) {
   // are scaled back before the cluster sums them: power-of-two scalings are exact, so the logits
   // are the same bits as with one scale for the whole row)
   const bool onepass = ONEPASS_C && !stage4k;
+  constexpr bool STAGER_C = !STAGE4K_C && (VAR == 0 || VAR == 3 || VAR == 4) &&
+                            XF == TFD_X_BF16 && !AQ && NT == 1 && KSL == 4;
+  // (measured faster where the general loop would take two passes; slower for one)
+  const bool stager = STAGER_C && spad * STEPK / 8 > kThreads && spad * STEPK / 8 <= 2 * kThreads;
   if constexpr (!STAGE4K_C) TFD_STAMP(a.trace, 57);  // general staging: after the first barrier
   if (F16 && !onepass && !stage4k) {
     if (F16) {
@@ -833,6 +837,73 @@ gemv_kernel(const GemvArgs a) {
     TFD_STAMP(a.trace, 59);
 #pragma unroll
     for (int r = 0; r < 8 * NT; ++r) xs[((s * NT + (r >> 3)) * H + hf) * 32 + (r & 7) * 4 + tt] = v[r];
+  } else if (STAGER_C && stager) {
+    // one n-tile, a block k range of 513-1024 chunks a row (small matrices, e.g. the pass's
+    // 11008-wide projection): like the 4096-wide form, every chunk a thread owns (two) loaded at
+    // once for all rows, the block's row maxima and f16 conversion in registers, one store a slot
+    constexpr int CPT = 2;
+    const int cpr = spad * STEPK / 8;
+    uint4 v[CPT][8];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+      const int c = tid + i * kThreads;
+      const int64_t kg = (int64_t)kstep0 * STEPK + 8 * c;
+      const bool kin = c < cpr && kg < K;
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        v[i][r] = (kin && r < rows) ? *reinterpret_cast<const uint4*>(
+                                          reinterpret_cast<const uint16_t*>(a.x) + (int64_t)r * a.ldx + kg)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (csplit > 1) l2_prefetch();
+    TFD_STAMP(a.trace, 57);
+    if (F16) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r < rows) {  // block-uniform
+          uint32_t m = 0u;
+#pragma unroll
+          for (int i = 0; i < CPT; ++i) {
+            const uint32_t w[4] = {v[i][r].x, v[i][r].y, v[i][r].z, v[i][r].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m = max(m, max((w[j] << 16) & 0x7FFFFFFFu, w[j] & 0x7FFF0000u));
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == 0 && m != 0u) atomicMax(&sxmax[r], m);
+        }
+      }
+      __syncthreads();
+      row_scales_from_max();
+      TFD_STAMP(a.trace, 58);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float inv = __uint_as_float(sxmax[r]);
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+          const uint32_t w[4] = {v[i][r].x, v[i][r].y, v[i][r].z, v[i][r].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o[j]) : "f"(bf16_hi(w[j]) * inv), "f"(bf16_lo(w[j]) * inv));
+          v[i][r] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+    TFD_STAMP(a.trace, 59);
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+      const int c = tid + i * kThreads;
+      if (c < cpr) {
+        const int k0 = 8 * c;
+        const int s = k0 / STEPK;
+        const int rem = k0 - s * STEPK;
+        const int tt = BLK ? (rem & 31) >> 3 : rem / E;
+        const int hf = BLK ? rem >> 5 : (rem - tt * E) >> 3;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) xs[(s * H + hf) * 32 + r * 4 + tt] = v[i][r];
+      }
+    }
   } else
   // Chunk (r, c) (8 consecutive k of activation row r at column c of this block's k range) goes to
   // one 16-byte fragment slot. Thread tid takes columns tid, tid + 512, ... (a block-uniform loop),
